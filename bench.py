@@ -1,0 +1,366 @@
+"""Benchmark of the layer-staged eager decode step on GB300.
+
+One step = one decode step of the whole trunk (embed, every layer's
+RMSNorm+QKV+RoPE+KV append, split-K attention, o-proj+residual,
+RMSNorm+gate/up+SwiGLU, down+residual, the boundary hand-overs, the final
+norm + LM head) for the batch, teacher forced.
+
+Default workload: the 8B-shape decoder (32 layers, n_embd 4096, 32 q / 8 kv
+heads, head_dim 128, ffn 14336, vocab 128256), bf16 weights and KV cache,
+batch 1, 4 stages (cuts 8, 16, 24), context 8192, 256 decode steps, deferred
+logits readback. Weights are seeded N(0, 0.02) (synthetic: no checkpoint);
+the context's cache rows are filled synthetically (their values do not change
+the time); the weights (15 GB) are far larger than L2, so every step streams
+them from HBM.
+
+Prints one JSON line. ``--impl reference`` times the CPU oracle on the same
+workload instead (host cores).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s and achieved HBM GB/s (% of 8 TB/s) per step, 1×GB300"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--config", default="8b")
+    ap.add_argument("--ctx", type=int, default=None, help="context length before the timed steps")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fill", default="synthetic", choices=["synthetic", "decode"])
+    return ap.parse_args()
+
+
+def workload_name(cfg, ctx, steps, readback="deferred"):
+    return (f"{cfg.name}-shape decoder: {cfg.n_layers} layers, n_embd {cfg.n_embd}, {cfg.q_heads} q / "
+            f"{cfg.kv_heads} kv heads, head_dim {cfg.head_dim}, ffn {cfg.ffn}, vocab {cfg.vocab}, "
+            f"{cfg.weight_dtype} weights, bf16 KV, batch {cfg.batch}, context {ctx}, {steps} decode steps, "
+            f"{len(cfg.fence) - 1} stages (cuts {','.join(map(str, cfg.cuts))}), {readback} readback")
+
+
+def dtype_of(cfg):
+    return "int8" if cfg.weight_dtype == "int8" else "bf16"
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_traffic(kind: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it still matches the kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        data = json.load(open(path))
+    except Exception:
+        return None
+    ent = data.get(kind)
+    if not ent or ent.get("workload") != workload:
+        return None
+    src = open(os.path.join(ROOT, "layer_pipeline_staged_gb300", "csrc", ent["source"]), "rb").read()
+    if hashlib.sha256(src).hexdigest()[:16] != ent.get("source_sha256_16"):
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.device = device
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.device), f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.p:
+            time.sleep(0.25)
+            self.p.terminate()
+            try:
+                self.out = self.p.communicate(timeout=5)[0]
+            except Exception:
+                self.p.kill()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append(parts)
+            except Exception:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_baseline(cfg, w, ctx: int, budget_s: float):
+    """The oracle as it stands, on this host's cores, at the workload's context
+    (cache filled synthetically: contents do not change the time)."""
+    import oracle
+    import synth
+    orc = oracle.Oracle(cfg, w, max_ctx=ctx + 64)
+    zeros = np.zeros((cfg.kv_heads, ctx + 64, cfg.head_dim), np.uint16)
+    for l in range(cfg.n_layers):
+        for b in range(cfg.batch):
+            orc.kv_import(l, b, zeros, zeros, ctx)
+    toks = synth.make_tokens(cfg, 64, seed=cfg.seed_t + 17)
+    n, t0 = 0, time.perf_counter()
+    while n < 64:
+        orc.step(toks[n], ctx + n)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s and n >= 2:
+            break
+    dt = time.perf_counter() - t0
+    threads = orc.L.orc_get_threads()
+    orc.close()
+    return {"value": cfg.batch * n / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} decode steps at positions {ctx}..{ctx + n - 1} (batch {cfg.batch}) of the same workload, "
+                      f"cache filled synthetically; {dt:.1f} s of CPU work"}
+
+
+def run_reference(args, cfg, ctx):
+    """The reference arm: the CPU oracle on the same workload, bounded sample per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import synth
+    t_gen = time.perf_counter()
+    w = synth.make_weights(cfg)
+    gen_s = time.perf_counter() - t_gen
+    import oracle
+    orc = oracle.Oracle(cfg, w, max_ctx=ctx + args.steps + args.warmup + 2)
+    zeros = np.zeros((cfg.kv_heads, ctx + args.steps + args.warmup + 2, cfg.head_dim), np.uint16)
+    for l in range(cfg.n_layers):
+        for b in range(cfg.batch):
+            orc.kv_import(l, b, zeros, zeros, ctx - args.warmup)
+    toks = synth.make_tokens(cfg, args.steps + args.warmup, seed=cfg.seed_t + 17)
+    for i in range(min(args.warmup, 1)):
+        orc.step(toks[i], ctx - args.warmup + i)
+    # bounded sample: at most ~60 s of oracle steps, each one full step of the workload
+    n, t0 = 0, time.perf_counter()
+    pos0 = ctx - args.warmup + min(args.warmup, 1)
+    while n < args.steps:
+        orc.step(toks[min(args.warmup, 1) + n], pos0 + n)
+        n += 1
+        if time.perf_counter() - t0 > 60.0 and n >= 2:
+            break
+    dt = time.perf_counter() - t0
+    v = cfg.batch * n / dt
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / n, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype_of(cfg), "data": "synthetic",
+            "config": {"workload": workload_name(cfg, ctx, args.steps), "parallelism": "stages on one device"},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": orc.L.orc_get_threads(), "kind": "oracle",
+                             "sample": f"{n} of {args.steps} decode steps at positions {pos0}..{pos0 + n - 1}, "
+                                       f"cache filled synthetically (weights drawn in {gen_s:.0f} s, untimed)"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    import synth
+    cfg = synth.CONFIGS[args.config]
+    ctx = args.ctx if args.ctx is not None else cfg.ctx
+    if args.impl == "reference":
+        run_reference(args, cfg, ctx)
+        return
+
+    import torch
+    import layer_pipeline_staged_gb300 as lps
+    from layer_pipeline_staged_gb300 import build as lps_build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        dist = None
+    torch.cuda.set_device(local)
+    lps_build.build()
+
+    K, W = args.steps, args.warmup
+    max_ctx = ctx + K
+    w = synth.make_weights(cfg)
+    desc = dict(n_layers=cfg.n_layers, n_embd=cfg.n_embd, n_q_heads=cfg.q_heads, n_kv_heads=cfg.kv_heads,
+                head_dim=cfg.head_dim, ffn=cfg.ffn, vocab=cfg.vocab,
+                weight_dtype=1 if cfg.weight_dtype == "int8" else 0, kv_dtype=0, max_ctx=max_ctx,
+                batch=cfg.batch, pending_depth=4, rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps, flags=0)
+    plan = lps.stage_plan_create(cfg.n_layers, cuts=list(cfg.cuts))
+    model = lps.model_bind(plan, desc, w, device=local)
+    B, V = cfg.batch, cfg.vocab
+    toks = synth.make_tokens(cfg, W + K)
+    start = ctx - W
+    # context rows [0, start): synthetic cache contents, or teacher-forced decode steps
+    if args.fill == "synthetic" and start > 0:
+        for l in range(cfg.n_layers):
+            for b in range(B):
+                k = synth.uniform_bf16(cfg.seed_t + 5, 2 * (l * B + b), (cfg.kv_heads, max_ctx, cfg.head_dim))
+                v = synth.uniform_bf16(cfg.seed_t + 5, 2 * (l * B + b) + 1, (cfg.kv_heads, max_ctx, cfg.head_dim))
+                model.kv_import(l, b, k, v, start)
+    elif start > 0:
+        ftoks = synth.make_tokens(cfg, start, seed=cfg.seed_t + 9)
+        tdev = torch.tensor(ftoks, dtype=torch.int32, device="cuda")
+        scratch = torch.empty((B, V), dtype=torch.float32, device="cuda")
+        for t in range(start):
+            model.decode_step_device(tdev[t].data_ptr(), t, scratch.data_ptr())
+        model.synchronize()
+
+    tok_dev = torch.tensor(toks, dtype=torch.int32, device="cuda")
+    logits_dev = torch.empty((B, V), dtype=torch.float32, device="cuda")
+    s_first = torch.cuda.ExternalStream(model.stream(0))
+    s_last = torch.cuda.ExternalStream(model.stream(plan.n_stages - 1))
+
+    def device_pass(first_pos):
+        for i in range(K):
+            model.decode_step_device(tok_dev[W + i].data_ptr(), first_pos + i, logits_dev.data_ptr())
+
+    # warm-up steps at positions start .. ctx-1
+    for i in range(W):
+        model.decode_step_device(tok_dev[i].data_ptr(), start + i, logits_dev.data_ptr())
+    model.synchronize()
+
+    def barrier():
+        if dist:
+            dist.barrier()
+
+    # ---- timed region: inputs resident in HBM, K steps at positions ctx .. ctx+K-1
+    launches0 = model.stats()["kernel_launches"]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        model.synchronize()
+        ev0.record(s_first)
+        device_pass(ctx)
+        ev1.record(s_last)
+        ev1.synchronize()
+        torch.cuda.synchronize()
+        barrier()
+        elapsed_ms = ev0.elapsed_time(ev1)
+        launches = model.stats()["kernel_launches"] - launches0
+
+        # ---- e2e: the public API with host buffers (tokens in, logits out), deferred pipelined
+        depth = 4
+        host_logits = np.empty((B, V), np.float32)
+        barrier()
+        model.synchronize()
+        t0 = time.perf_counter()
+        pend = []
+        for i in range(K):
+            pend.append(model.decode_step_deferred(toks[W + i], ctx + i))
+            if len(pend) == depth:
+                p = pend.pop(0)
+                p.wait(out=host_logits)
+                p.free()
+        for p in pend:
+            p.wait(out=host_logits)
+            p.free()
+        e2e_s = time.perf_counter() - t0
+        barrier()
+
+        # ---- dominant kernel timed live with CUDA events on its stage stream (same steps again)
+        dom = "gateup"
+        model.time_kernel(dom, True)
+        device_pass(ctx)
+        dom_ms, dom_n = model.kernel_time(dom)
+        model.time_kernel(dom, False)
+
+    if dist:
+        t = torch.tensor([elapsed_ms, e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms, e2e_s = float(t[0]), float(t[1])
+    n = world
+    tok_s = n * B * K / (elapsed_ms / 1e3)
+    step_bytes = [cfg.step_bytes(ctx + i) for i in range(K)]
+    hbm_gbs = sum(step_bytes) / (elapsed_ms / 1e3) / 1e9
+    peaks, peak_src = measured_peaks()
+    dom_bytes = 2 * cfg.ffn * cfg.n_embd * (1 if cfg.weight_dtype == "int8" else 2)
+    dom_bytes += cfg.n_embd * 4 * 2 + cfg.ffn * 4  # h and gain in, SwiGLU activations out
+    if cfg.weight_dtype == "int8":
+        dom_bytes += 2 * cfg.ffn * 4
+    dom_avg_s = dom_ms / 1e3 / max(dom_n, 1)
+    achieved = dom_bytes / dom_avg_s / 1e9
+    wl = workload_name(cfg, ctx, K)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, w, ctx, args.cpu_seconds)
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": n, "steps": K, "warmup": W,
+        "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": dtype_of(cfg), "data": "synthetic",
+        "config": {"workload": wl, "l2": "inputs larger than L2 (every step streams all weights from HBM)",
+                   "cache_fill": args.fill, "parallelism": f"{plan.n_stages} stages on one device"
+                   + (f", {n} independent replicas" if n > 1 else "")},
+        "hbm_gbs": hbm_gbs, "hbm_frac_of_8tbs": hbm_gbs / NOMINAL_HBM_GBS,
+        "hbm_frac_of_measured": hbm_gbs / peaks["hbm_gbs"],
+        "bytes_per_step": sum(step_bytes) / K,
+        "roofline": {"kernel": "RMSNorm + gate/up GEMV + SwiGLU (per layer, 54% of step bytes)", "bound": "hbm",
+                     "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
+                     else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_us": dom_avg_s * 1e6,
+                     "launches_timed": dom_n, "traffic": kernel_traffic(dom, wl)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": n * B * K / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": B * 8,
+                "d2h_bytes_per_step": B * V * 4,
+                "how": "decode_step_deferred + pending_wait with host token ids and host logits, 4 steps in flight"},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    model.close()
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,248 @@
+/*
+ * lps.h -- C ABI of the layer-staged eager decode step on one GB300 (sm_103a).
+ *
+ * One eager decode step of a decoder-only transformer trunk whose layers are
+ * split into N contiguous stages, all on one GPU (the repeated-device-id mode
+ * of ninfer's pipeline-stages.md, "What it is and is not": `--devices 0,0`).
+ * Each stage owns its layers' weights, KV cache and scratch and runs on its own
+ * CUDA stream; the f32 hidden state [n_embd] is the only tensor that crosses a
+ * stage boundary, through two persistent slots per boundary ordered by ev_tx /
+ * ev_rx events (memra_engine::pp module docs, "M2 increment 1" and "Ownership
+ * across a boundary"). Logits are read back eagerly or deferred on a dedicated
+ * readback stream ("M2 increment 3", PendingLogits).
+ *
+ * Conventions for every call:
+ *   - return 0 (LPS_OK) on success, a negative LPS_E* code on failure;
+ *     last_error_string() then names the refusing call and the reason;
+ *   - arguments are checked before any GPU work is enqueued; a refused call
+ *     changes no state ("fail closed": memra_engine::pp, refuse_unsplit_if_remote);
+ *   - pointers marked "host" are ordinary CPU memory owned by the caller and
+ *     only read or written during the call; pointers marked "device" are
+ *     device memory on the model's GPU;
+ *   - a model is driven from one host thread at a time.
+ */
+#ifndef LPS_H
+#define LPS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- error codes ------------------------------------------------------- */
+#define LPS_OK 0
+#define LPS_EINVAL (-1)    /* bad argument: cuts, shapes, token >= vocab, pos out of range, ... */
+#define LPS_ENOMEM (-2)    /* a device or pinned-host allocation failed */
+#define LPS_ECUDA (-3)     /* a CUDA call failed, or a kernel reported a device-side error;
+                              the model is then unusable and must be destroyed */
+#define LPS_ETIMEDOUT (-4) /* pending_wait ran out of time; the pending handle stays valid */
+#define LPS_EBUSY (-5)     /* every deferred-readback slot is held by an unfreed pending handle */
+
+/* ---- opaque handles ---------------------------------------------------- */
+typedef struct lps_stage_plan lps_stage_plan;
+typedef struct lps_model lps_model;
+typedef struct lps_pending lps_pending;
+
+/* ---- stage plan (host only, no GPU needed) ----------------------------- */
+
+/* Build the stage fence of a trunk of n_layers layers from N-1 cuts
+ * (memra_engine::pp, "Door": cuts strictly increasing, each in (0, n_layers);
+ * pp_cuts: fence = [0, c1, .., cN-1, n_layers], stage s runs layers
+ * [fence[s], fence[s+1])).
+ *   cuts    host int[n_cuts], or NULL for the even split into n_cuts+1 stages,
+ *           cut s = s * n_layers / (n_cuts + 1) (integer division);
+ *   n_cuts  N-1 >= 0;
+ *   out     receives a new plan, owned by the caller (stage_plan_destroy).
+ * LPS_EINVAL if the cuts are not strictly increasing in (0, n_layers) or the
+ * even split would leave a stage empty. */
+int stage_plan_create(int n_layers, const int* cuts, int n_cuts, lps_stage_plan** out);
+
+/* The same plan spelled as layer counts per stage (ninfer pipeline-stages.md,
+ * "How it works": `--stage-layers 30,34`). counts: host int[n_stages], each >= 1. */
+int stage_plan_from_counts(const int* counts, int n_stages, lps_stage_plan** out);
+
+void stage_plan_destroy(lps_stage_plan* plan);
+
+/* Number of stages N (>= 1). */
+int stage_plan_n_stages(const lps_stage_plan* plan);
+
+/* Copy the fence (N+1 ints) into host fence[cap]; returns N+1, or LPS_EINVAL if cap < N+1. */
+int stage_plan_fence(const lps_stage_plan* plan, int* fence, int cap);
+
+/* The stage that owns layer il (memra_engine::pp, stage_of); LPS_EINVAL if il is out of range. */
+int stage_of(const lps_stage_plan* plan, int il);
+
+/* ---- model description and weights ------------------------------------- */
+#define LPS_WEIGHT_BF16 0          /* bf16 weights */
+#define LPS_WEIGHT_INT8_ROWSCALE 1 /* int8 weights with one fp32 scale per output row: w = q * s_row */
+#define LPS_KV_BF16 0              /* bf16 KV cache */
+
+#define LPS_FLAG_SINGLE_STREAM 1u  /* test arm: every stage on one stream, each boundary two plain
+                                      device-to-device copies (memra_engine::pp, pp2_streams_off) */
+#define LPS_FLAG_KEEP_ATTN_OUT 2u  /* keep each layer's attention output of the latest step
+                                      readable through model_attn_out (debug) */
+
+typedef struct lps_model_desc {
+  int n_layers;     /* trunk layers; must equal the plan's */
+  int n_embd;       /* d; multiple of 8 (16 for int8) */
+  int n_q_heads;    /* nq (the bound width, dummy heads included) */
+  int n_kv_heads;   /* nkv; nq % nkv == 0; q head h reads kv head h / (nq / nkv) */
+  int head_dim;     /* hd: 64 or 128 */
+  int ffn;          /* SwiGLU hidden width; multiple of 8 (16 for int8) */
+  int vocab;        /* V */
+  int weight_dtype; /* LPS_WEIGHT_* */
+  int kv_dtype;     /* LPS_KV_BF16 */
+  int max_ctx;      /* cache rows per (layer, sequence, kv head) */
+  int batch;        /* B independent sequences per step, 1..8 */
+  int pending_depth;/* deferred-readback slots; 0 means 4 */
+  float rope_theta; /* RoPE base (rotate-half pairs (i, i + hd/2), angle pos * theta^(-2i/hd)) */
+  float rms_eps;    /* RMSNorm epsilon: xn = h * g / sqrt(mean(h^2) + eps) */
+  uint32_t flags;   /* LPS_FLAG_* */
+} lps_model_desc;
+
+/* A host weight matrix [rows, cols], row-major (output row r, input column k).
+ * w: bf16 bit patterns (uint16) or int8 values; scale: host float[rows] for
+ * LPS_WEIGHT_INT8_ROWSCALE, else ignored. */
+typedef struct lps_matrix {
+  const void* w;
+  const float* scale;
+} lps_matrix;
+
+typedef struct lps_layer_weights {
+  const float* attn_norm; /* [n_embd] fp32 RMSNorm gain before attention */
+  lps_matrix wq;          /* [nq*hd, n_embd], rows head-major (row = head*hd + i) */
+  lps_matrix wk;          /* [nkv*hd, n_embd] */
+  lps_matrix wv;          /* [nkv*hd, n_embd] */
+  lps_matrix wo;          /* [n_embd, nq*hd] */
+  const float* ffn_norm;  /* [n_embd] */
+  lps_matrix w_gate;      /* [ffn, n_embd] */
+  lps_matrix w_up;        /* [ffn, n_embd] */
+  lps_matrix w_down;      /* [n_embd, ffn] */
+} lps_layer_weights;
+
+typedef struct lps_model_weights {
+  lps_matrix embed;                /* [vocab, n_embd]: h = E[token] (stage 0 owns it) */
+  const float* out_norm;           /* [n_embd] final RMSNorm gain (last stage) */
+  lps_matrix lm_head;              /* [vocab, n_embd] untied head (last stage) */
+  const lps_layer_weights* layers; /* [n_layers] */
+} lps_model_weights;
+
+/* Optional runtime hooks. alloc/free route every device allocation of the
+ * model (weights, caches, scratch, slots) to the caller, e.g. PyTorch's
+ * caching allocator; alloc must return 256-byte-aligned device memory or NULL.
+ * streams, if not NULL, holds N+1 cudaStream_t handles: one per stage, then
+ * the readback stream; the caller keeps them alive until model_destroy. */
+typedef void* (*lps_alloc_fn)(void* ctx, size_t bytes);
+typedef void (*lps_free_fn)(void* ctx, void* ptr);
+typedef struct lps_runtime {
+  int device;          /* CUDA device ordinal */
+  lps_alloc_fn alloc;  /* NULL: cudaMalloc */
+  lps_free_fn free;    /* required when alloc is set */
+  void* alloc_ctx;
+  void* const* streams;/* NULL: the model creates its own non-blocking streams */
+} lps_runtime;
+
+/* Upload a model onto one GPU, placed per stage: stage s holds the weights,
+ * KV cache ([layers of s][B][nkv][max_ctx][hd] bf16) and scratch of its
+ * layers; the embedding goes with stage 0, the final norm and LM head with
+ * the last stage (memra_engine::pp, layer_engine and new_cache). The weights
+ * are copied (the caller may free them on return); the load ends with one
+ * synchronize per stage (memra_engine::pp, sync_stages_after_load).
+ *   plan  a stage plan whose n_layers equals desc->n_layers (not retained);
+ *   rt    optional runtime hooks, or NULL (device 0, cudaMalloc, own streams).
+ * LPS_EINVAL for unsupported shapes, LPS_ENOMEM / LPS_ECUDA on device failure
+ * (everything allocated so far is released). */
+int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc, const lps_model_weights* w,
+               const lps_runtime* rt, lps_model** out);
+
+/* Drain every stream and free the model; outstanding pending handles become
+ * invalid (free them first). NULL is a no-op. */
+void model_destroy(lps_model* m);
+
+/* ---- the decode step --------------------------------------------------- */
+
+/* One eager decode step for every sequence b: token tokens[b] at position
+ * pos[b]. Writes KV row pos[b] of every layer, attends over rows [0, pos[b]],
+ * and copies the logits to host logits[B][vocab] (fp32, caller-owned) before
+ * returning. Requires 0 <= tokens[b] < vocab and 0 <= pos[b] <= filled[b]
+ * (the rows written so far; rewinding is allowed, holes are not) and
+ * pos[b] < max_ctx; afterwards filled[b] = pos[b] + 1. */
+int decode_step(lps_model* m, const int32_t* tokens, const int32_t* pos, float* logits);
+
+/* The same step, ending without the logits copy (memra_engine::pp,
+ * decode_step_h_ppn_deferred): the logits stay on the device with a
+ * completion event and *out receives a pending handle. Later steps may be
+ * enqueued before it is waited. LPS_EBUSY if all pending_depth slots are held. */
+int decode_step_deferred(lps_model* m, const int32_t* tokens, const int32_t* pos, lps_pending** out);
+
+/* Wait for a deferred step and copy its logits to host logits[B][vocab]: the
+ * readback stream waits the step's completion event, copies and synchronizes
+ * (memra_engine::pp, PendingLogits::wait). timeout_ms < 0 waits without limit;
+ * LPS_ETIMEDOUT leaves the handle valid. A handle may be waited more than once. */
+int pending_wait(lps_pending* p, float* logits, int timeout_ms);
+
+/* Release a pending handle, waited or not (dropping without waiting is safe). */
+void pending_free(lps_pending* p);
+
+/* The step with device-resident input and output: tokens is a device int[B],
+ * pos a host int[B] (the per-step position snapshot), logits a device
+ * float[B][vocab]. Returns once the step is enqueued; the logits are ready
+ * when model_synchronize returns or after work ordered on the stream that
+ * model_stream(m, N-1) returns. */
+int decode_step_device(lps_model* m, const int32_t* tokens, const int32_t* pos, float* logits);
+
+/* Block until every stream of the model is idle; reports device-side errors. */
+int model_synchronize(lps_model* m);
+
+/* The cudaStream_t of stage s (0..N-1) or of the readback stream (s = N). */
+int model_stream(const lps_model* m, int s, void** stream);
+
+/* ---- errors, counters, test hooks ---------------------------------------- */
+
+/* Thread-local message of the last failure on this thread ("" if none). */
+const char* last_error_string(void);
+
+typedef struct lps_stats {
+  uint64_t steps;              /* decode steps enqueued (all entry points) */
+  uint64_t deferred_steps;     /* of which deferred */
+  uint64_t stage_walks;        /* per-stage layer walks enqueued (N per step) */
+  uint64_t boundary_crossings; /* hidden-state hand-overs across a cut (N-1 per step) */
+  uint64_t pending_drains;     /* completed pending_wait readbacks */
+  uint64_t kernel_launches;    /* this library's kernel launches */
+  int n_stages;
+  int fence[17];               /* the first min(N, 16)+1 entries of the fence */
+} lps_stats;
+
+int model_stats(const lps_model* m, lps_stats* out);
+
+/* Copy the cache rows of (layer, sequence b) out of or into the device:
+ * host buffer [2][nkv][max_ctx][hd] bf16 (K then V), bytes must equal
+ * 4 * nkv * max_ctx * hd. Import also sets filled[b] = filled (0..max_ctx).
+ * Both synchronize the owning stage's stream. */
+int model_kv_export(const lps_model* m, int layer, int b, void* host, size_t bytes);
+int model_kv_import(lps_model* m, int layer, int b, const void* host, size_t bytes, int filled);
+
+/* Attention output of (layer, sequence b) in the latest step, host float[nq*hd];
+ * needs LPS_FLAG_KEEP_ATTN_OUT. */
+int model_attn_out(const lps_model* m, int layer, int b, float* host);
+
+/* Per-kernel timing with CUDA events on the launching stream, for the kernel
+ * family `kind` (LPS_KERNEL_*). Enabling starts a new measurement; reading
+ * synchronizes and returns the summed device time and launch count. */
+#define LPS_KERNEL_QKV 0
+#define LPS_KERNEL_ATTN 1
+#define LPS_KERNEL_OPROJ 2
+#define LPS_KERNEL_GATEUP 3
+#define LPS_KERNEL_DOWN 4
+#define LPS_KERNEL_HEAD 5
+#define LPS_KERNEL_EMBED 6
+int model_time_kernel(lps_model* m, int kind, int enable);
+int model_kernel_time(lps_model* m, int kind, double* total_ms, uint64_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LPS_H */

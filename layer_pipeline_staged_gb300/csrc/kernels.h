@@ -1,0 +1,85 @@
+// Kernel parameter blocks and host-side launchers of the decode-step kernels.
+// Shapes are validated by the runtime before any launcher is called.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lps {
+
+constexpr int kMaxBatch = 8;
+
+// ---- weight-streaming GEMV (batch 1) --------------------------------------
+// y = W x over a row-major weight matrix whose rows are grouped into "units"
+// of unit_rows consecutive rows (1, or 2 for a RoPE pair / a gate-up pair).
+// Rows are packed at bind time so that every unit, and every CTA's range of
+// units, is one contiguous byte range streamed by 1D bulk copies.
+enum GemvEpilogue : int {
+  kEpiQkv = 0,     // unit = (row i, row i + hd/2) of one head: RoPE, q out, K/V cache append
+  kEpiResidual = 1,// unit = 1 row: h_out[r] = h_in[r] + y
+  kEpiSwiglu = 2,  // unit = (gate_i, up_i): a[i] = silu(gate) * up
+  kEpiStore = 3,   // unit = 1 row: out[r] = y (logits)
+};
+
+struct GemvParams {
+  const void* w;        // packed weights [rows][K] (bf16 or int8)
+  const float* wscale;  // int8: per packed row scale; else nullptr
+  int rows, K;
+  int unit_rows, units;
+  int units_per_buf, nbuf;
+  // input vector: either x (used as is) or rmsnorm(h) * gain
+  const float* x;
+  const float* h;
+  const float* gain;
+  float eps;
+  // epilogue
+  float* out;           // q [nq*hd] | a [ffn] | logits [rows]
+  const float* h_in;    // residual input (may alias h_out)
+  float* h_out;
+  __nv_bfloat16* kc;    // K cache of this layer and sequence: [nkv][max_ctx][hd]
+  __nv_bfloat16* vc;
+  const float2* rope;   // (cos, sin) [hd/2] at this step's position
+  int nq, nkv, hd, max_ctx, pos;
+  int* status;
+};
+
+struct GemvPlan {
+  int grid, smem, units_per_buf, nbuf;
+};
+GemvPlan gemv_plan(int rows, int K, int unit_rows, bool int8, int num_sms);
+cudaError_t launch_gemv(const GemvParams& p, int epi, bool norm, bool int8, const GemvPlan& plan,
+                        cudaStream_t s, bool pdl);
+
+// ---- split-K GQA decode attention -----------------------------------------
+struct AttnParams {
+  const float* q;              // [B][nq*hd]
+  const __nv_bfloat16* kc;     // layer base: [B][nkv][max_ctx][hd]
+  const __nv_bfloat16* vc;
+  float* out;                  // [B][nq*hd]
+  float* part;                 // scratch [B][nq][max_chunks][hd + 2]
+  int* counter;                // scratch [B][nkv], zero between launches
+  int nq, nkv, hd, max_ctx, max_chunks;
+  int chunk;                   // positions per CTA (multiple of the sub-tile)
+  int pos[kMaxBatch];
+  float scale;                 // 1/sqrt(hd)
+  int* status;
+};
+int attn_sub_tile(int hd);
+int attn_chunk(int hd, int nkv, int batch, int max_pos, int num_sms);
+int attn_max_chunks(int hd, int nkv, int batch, int max_ctx, int num_sms);
+cudaError_t launch_attention(const AttnParams& p, int batch, int max_pos, cudaStream_t s, bool pdl);
+
+// ---- embedding -------------------------------------------------------------
+struct EmbedParams {
+  const void* table;     // [vocab][d] bf16 or int8
+  const float* scale;    // int8 row scales
+  const int* tok_dev;    // device tokens, or nullptr to use tok[]
+  int tok[kMaxBatch];
+  int d, vocab, batch;
+  float* h;              // [B][d]
+  int* status;
+};
+cudaError_t launch_embed(const EmbedParams& p, bool int8, cudaStream_t s, bool pdl);
+
+}  // namespace lps

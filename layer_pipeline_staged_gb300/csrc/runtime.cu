@@ -1,0 +1,1116 @@
+// Host runtime behind the C ABI of include/lps.h: stage plans, per-stage
+// placement and upload, the step schedule across per-stage streams with
+// double-buffered boundary slots ordered by ev_tx / ev_rx events, eager and
+// deferred logits readback, counters and test hooks.
+//
+// Structure follows the pages' N-stage runtime (memra_engine::pp): per-stage
+// execution homes (StageRt: stream + stage-owned weights, cache and scratch),
+// N-1 boundaries with two persistent slots each and their own step counter,
+// the fence of pp_cuts, the load barrier of sync_stages_after_load and the
+// PendingLogits readback on a dedicated stream. Differences from the pages'
+// design: one device and one context; every buffer is allocated at bind
+// (nothing is allocated per step); the hand-over is fused into the kernels
+// (the last layer of stage s writes its residual output straight into the
+// boundary slot and stage s+1's first layer reads it from there); and all
+// shared mutable state of a step is per stage, so stages of consecutive
+// steps can overlap on one device.
+#include <cuda_runtime.h>
+
+#include <chrono>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "kernels.h"
+#include "lps.h"
+
+namespace lps {
+bool gemv_supported(int K, int unit_rows, bool int8);
+bool attn_supported(int hd, int group);
+}  // namespace lps
+
+using namespace lps;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fn, const std::string& why) {
+  g_err = std::string(fn) + ": " + why;
+  return code;
+}
+
+int cuda_fail(const char* fn, const char* what, cudaError_t e) {
+  return fail(LPS_ECUDA, fn, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define CK(expr, what)                                   \
+  do {                                                   \
+    cudaError_t e_ = (expr);                             \
+    if (e_ != cudaSuccess) return cuda_fail(FN, what, e_); \
+  } while (0)
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// stage plan
+// ---------------------------------------------------------------------------
+
+struct lps_stage_plan {
+  int n_layers;
+  std::vector<int> fence;  // N+1 entries
+};
+
+extern "C" int stage_plan_create(int n_layers, const int* cuts, int n_cuts, lps_stage_plan** out) {
+  static const char* FN = "stage_plan_create";
+  if (!out) return fail(LPS_EINVAL, FN, "out is NULL");
+  *out = nullptr;
+  if (n_layers < 1) return fail(LPS_EINVAL, FN, "n_layers must be >= 1");
+  if (n_cuts < 0 || n_cuts >= n_layers) return fail(LPS_EINVAL, FN, "need 0 <= n_cuts < n_layers");
+  const int N = n_cuts + 1;
+  std::vector<int> fence(N + 1);
+  fence[0] = 0;
+  fence[N] = n_layers;
+  for (int s = 1; s < N; ++s) fence[s] = cuts ? cuts[s - 1] : static_cast<int>(static_cast<long long>(s) * n_layers / N);
+  for (int s = 0; s < N; ++s)
+    if (fence[s + 1] <= fence[s])
+      return fail(LPS_EINVAL, FN, "cuts must be strictly increasing and inside (0, n_layers)");
+  *out = new lps_stage_plan{n_layers, fence};
+  return LPS_OK;
+}
+
+extern "C" int stage_plan_from_counts(const int* counts, int n_stages, lps_stage_plan** out) {
+  static const char* FN = "stage_plan_from_counts";
+  if (!out) return fail(LPS_EINVAL, FN, "out is NULL");
+  *out = nullptr;
+  if (!counts || n_stages < 1) return fail(LPS_EINVAL, FN, "need counts and n_stages >= 1");
+  std::vector<int> fence(n_stages + 1, 0);
+  for (int s = 0; s < n_stages; ++s) {
+    if (counts[s] < 1) return fail(LPS_EINVAL, FN, "every stage needs at least one layer");
+    fence[s + 1] = fence[s] + counts[s];
+  }
+  *out = new lps_stage_plan{fence[n_stages], fence};
+  return LPS_OK;
+}
+
+extern "C" void stage_plan_destroy(lps_stage_plan* p) { delete p; }
+
+extern "C" int stage_plan_n_stages(const lps_stage_plan* p) {
+  if (!p) return fail(LPS_EINVAL, "stage_plan_n_stages", "plan is NULL");
+  return static_cast<int>(p->fence.size()) - 1;
+}
+
+extern "C" int stage_plan_fence(const lps_stage_plan* p, int* fence, int cap) {
+  static const char* FN = "stage_plan_fence";
+  if (!p || !fence) return fail(LPS_EINVAL, FN, "NULL argument");
+  const int n = static_cast<int>(p->fence.size());
+  if (cap < n) return fail(LPS_EINVAL, FN, "cap smaller than N+1");
+  std::memcpy(fence, p->fence.data(), sizeof(int) * n);
+  return n;
+}
+
+extern "C" int stage_of(const lps_stage_plan* p, int il) {
+  static const char* FN = "stage_of";
+  if (!p) return fail(LPS_EINVAL, FN, "plan is NULL");
+  if (il < 0 || il >= p->n_layers) return fail(LPS_EINVAL, FN, "layer out of range");
+  const int N = static_cast<int>(p->fence.size()) - 1;
+  for (int s = 0; s < N; ++s)
+    if (il < p->fence[s + 1]) return s;
+  return N - 1;
+}
+
+// ---------------------------------------------------------------------------
+// model
+// ---------------------------------------------------------------------------
+
+namespace {
+
+struct LayerDev {
+  void* w_qkv = nullptr;  // packed RoPE pairs: rows (head h, i) and (h, i + hd/2) adjacent
+  float* s_qkv = nullptr;
+  void* w_o = nullptr;
+  float* s_o = nullptr;
+  void* w_gu = nullptr;   // packed (gate_i, up_i) row pairs
+  float* s_gu = nullptr;
+  void* w_d = nullptr;
+  float* s_d = nullptr;
+  float* attn_norm = nullptr;
+  float* ffn_norm = nullptr;
+  __nv_bfloat16* kc = nullptr;  // [B][nkv][max_ctx][hd]
+  __nv_bfloat16* vc = nullptr;
+  float* o_keep = nullptr;      // [B][nq*hd] with LPS_FLAG_KEEP_ATTN_OUT
+};
+
+struct StageDev {
+  int l0 = 0, l1 = 0;
+  cudaStream_t stream = nullptr;
+  bool own_stream = false;
+  std::vector<LayerDev> layers;
+  float* h = nullptr;      // [B][d] this stage's residual stream
+  float* q = nullptr;      // [B][nq*hd]
+  float* o = nullptr;      // [B][nq*hd]
+  float* a = nullptr;      // [B][ffn]
+  float* part = nullptr;   // attention partials
+  int* counter = nullptr;  // attention chunk counters [B][nkv]
+  float2* rope = nullptr;  // [max_ctx][hd/2] (cos, sin)
+  void* embed = nullptr;   // stage 0
+  float* embed_s = nullptr;
+  void* head = nullptr;    // last stage
+  float* head_s = nullptr;
+  float* out_norm = nullptr;
+  GemvPlan plan_qkv{}, plan_o{}, plan_gu{}, plan_d{}, plan_head{};
+};
+
+struct Boundary {
+  float* slot[2] = {nullptr, nullptr};  // [B][d] f32
+  cudaEvent_t ev_tx[2] = {nullptr, nullptr};
+  cudaEvent_t ev_rx[2] = {nullptr, nullptr};
+  uint64_t steps = 0;
+};
+
+struct PendingSlot {
+  float* logits_dev = nullptr;
+  float* host = nullptr;  // pinned [B][V]
+  int* status_host = nullptr;
+  cudaEvent_t ev_done = nullptr;
+  bool held = false;
+  bool drained = false;
+  uint64_t step = 0;
+};
+
+struct KTimer {
+  bool on = false;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev;
+  size_t used = 0;
+  double total_ms = 0;
+  uint64_t launches = 0;
+};
+
+}  // namespace
+
+struct lps_model {
+  lps_model_desc d{};
+  int N = 0;
+  std::vector<int> fence;
+  int device = 0;
+  int num_sms = 0;
+  bool int8 = false;
+  bool single = false;
+  lps_alloc_fn alloc = nullptr;
+  lps_free_fn free_fn = nullptr;
+  void* alloc_ctx = nullptr;
+  std::vector<void*> dev_allocs;
+  std::vector<void*> host_allocs;
+  std::vector<StageDev> st;
+  std::vector<Boundary> bd;
+  cudaStream_t rb = nullptr;
+  bool own_rb = false;
+  int* status_dev = nullptr;
+  int* status_host = nullptr;
+  std::vector<int> filled;
+  std::vector<PendingSlot> pend;
+  float* eager_logits_dev = nullptr;
+  float* eager_host = nullptr;
+  uint64_t step_count = 0;
+  lps_stats stats{};
+  bool failed = false;
+  int attn_max_chunks = 0;
+  KTimer timers[7];
+
+  cudaStream_t stream(int s) const { return single ? st[0].stream : st[s].stream; }
+};
+
+struct lps_pending {
+  lps_model* m;
+  int slot;
+  uint64_t step;
+};
+
+namespace {
+
+void* dev_alloc(lps_model* m, size_t bytes) {
+  if (bytes == 0) bytes = 256;
+  void* p = nullptr;
+  if (m->alloc) {
+    p = m->alloc(m->alloc_ctx, bytes);
+  } else if (cudaMalloc(&p, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    p = nullptr;
+  }
+  if (p) m->dev_allocs.push_back(p);
+  return p;
+}
+
+void* host_alloc(lps_model* m, size_t bytes) {
+  void* p = nullptr;
+  if (cudaHostAlloc(&p, bytes ? bytes : 16, cudaHostAllocDefault) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  m->host_allocs.push_back(p);
+  return p;
+}
+
+void release(lps_model* m) {
+  cudaSetDevice(m->device);
+  for (auto& s : m->st)
+    if (s.stream) cudaStreamSynchronize(s.stream);
+  if (m->rb) cudaStreamSynchronize(m->rb);
+  for (auto& b : m->bd)
+    for (int i = 0; i < 2; ++i) {
+      if (b.ev_tx[i]) cudaEventDestroy(b.ev_tx[i]);
+      if (b.ev_rx[i]) cudaEventDestroy(b.ev_rx[i]);
+    }
+  for (auto& p : m->pend)
+    if (p.ev_done) cudaEventDestroy(p.ev_done);
+  for (auto& t : m->timers)
+    for (auto& e : t.ev) {
+      cudaEventDestroy(e.first);
+      cudaEventDestroy(e.second);
+    }
+  for (void* p : m->dev_allocs) {
+    if (m->free_fn)
+      m->free_fn(m->alloc_ctx, p);
+    else
+      cudaFree(p);
+  }
+  for (void* p : m->host_allocs) cudaFreeHost(p);
+  for (auto& s : m->st)
+    if (s.own_stream && s.stream) cudaStreamDestroy(s.stream);
+  if (m->own_rb && m->rb) cudaStreamDestroy(m->rb);
+  cudaGetLastError();
+}
+
+// Double-buffered pinned staging for host -> device uploads on one stream.
+struct Uploader {
+  static constexpr size_t kCap = 64ull << 20;
+  void* buf[2] = {nullptr, nullptr};
+  cudaEvent_t ev[2] = {nullptr, nullptr};
+  int cur = 0;
+  size_t fill = 0;
+  char* dst = nullptr;  // device address of buf[cur]'s first byte
+  cudaStream_t s = nullptr;
+  cudaError_t err = cudaSuccess;
+
+  bool init() {
+    for (int i = 0; i < 2; ++i) {
+      if (cudaHostAlloc(&buf[i], kCap, cudaHostAllocDefault) != cudaSuccess) return false;
+      if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) return false;
+    }
+    return true;
+  }
+  ~Uploader() {
+    for (int i = 0; i < 2; ++i) {
+      if (ev[i]) {
+        cudaEventSynchronize(ev[i]);
+        cudaEventDestroy(ev[i]);
+      }
+      if (buf[i]) cudaFreeHost(buf[i]);
+    }
+  }
+  void flush() {
+    if (fill && err == cudaSuccess) {
+      err = cudaMemcpyAsync(dst, buf[cur], fill, cudaMemcpyHostToDevice, s);
+      if (err == cudaSuccess) err = cudaEventRecord(ev[cur], s);
+      cur ^= 1;
+      if (err == cudaSuccess) err = cudaEventSynchronize(ev[cur]);
+    }
+    fill = 0;
+    dst = nullptr;
+  }
+  // Copy `bytes` from host `src` to device `d` (contiguous), through staging.
+  void put(void* d, const void* src, size_t bytes) {
+    const char* sp = static_cast<const char*>(src);
+    char* dp = static_cast<char*>(d);
+    while (bytes) {
+      if (dst && (dst + fill != dp || fill == kCap)) flush();
+      if (!dst) dst = dp;
+      const size_t n = std::min(bytes, kCap - fill);
+      std::memcpy(static_cast<char*>(buf[cur]) + fill, sp, n);
+      fill += n;
+      sp += n;
+      dp += n;
+      bytes -= n;
+    }
+  }
+};
+
+size_t elem_bytes(const lps_model* m) { return m->int8 ? 1 : 2; }
+
+// Upload a [rows, cols] matrix whose device row r comes from host row src_row(r).
+template <class F>
+bool upload_rows(lps_model* m, Uploader& up, const lps_matrix& mat, int rows, int cols, void** w_dev,
+                 float** s_dev, F src_row) {
+  const size_t rb = static_cast<size_t>(cols) * elem_bytes(m);
+  *w_dev = dev_alloc(m, rb * rows);
+  if (!*w_dev) return false;
+  const char* src = static_cast<const char*>(mat.w);
+  for (int r = 0; r < rows; ++r) up.put(static_cast<char*>(*w_dev) + rb * r, src + rb * src_row(r), rb);
+  if (m->int8) {
+    *s_dev = static_cast<float*>(dev_alloc(m, sizeof(float) * rows));
+    if (!*s_dev) return false;
+    std::vector<float> s(rows);
+    for (int r = 0; r < rows; ++r) s[r] = mat.scale[src_row(r)];
+    up.put(*s_dev, s.data(), sizeof(float) * rows);
+    up.flush();
+  }
+  return up.err == cudaSuccess;
+}
+
+bool check_matrix(const lps_model* m, const lps_matrix& x) { return x.w && (!m->int8 || x.scale); }
+
+int timer_begin(lps_model* m, int kind, cudaStream_t s, cudaEvent_t* stop) {
+  *stop = nullptr;
+  KTimer& t = m->timers[kind];
+  if (!t.on) return 0;
+  if (t.used == t.ev.size()) {
+    cudaEvent_t a, b;
+    if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) return -1;
+    t.ev.emplace_back(a, b);
+  }
+  cudaEventRecord(t.ev[t.used].first, s);
+  *stop = t.ev[t.used].second;
+  ++t.used;
+  return 0;
+}
+
+void timer_end(lps_model* m, int kind, cudaStream_t s, cudaEvent_t stop) {
+  if (stop) {
+    cudaEventRecord(stop, s);
+    ++m->timers[kind].launches;
+  }
+}
+
+}  // namespace
+
+extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc, const lps_model_weights* w,
+                          const lps_runtime* rt, lps_model** out) {
+  static const char* FN = "model_bind";
+  if (!out) return fail(LPS_EINVAL, FN, "out is NULL");
+  *out = nullptr;
+  if (!plan || !desc || !w) return fail(LPS_EINVAL, FN, "plan, desc and weights are required");
+  const lps_model_desc& d = *desc;
+  if (d.n_layers != plan->n_layers) return fail(LPS_EINVAL, FN, "desc->n_layers differs from the plan's");
+  if (d.weight_dtype != LPS_WEIGHT_BF16 && d.weight_dtype != LPS_WEIGHT_INT8_ROWSCALE)
+    return fail(LPS_EINVAL, FN, "unsupported weight_dtype");
+  if (d.kv_dtype != LPS_KV_BF16) return fail(LPS_EINVAL, FN, "unsupported kv_dtype");
+  if (d.n_embd < 1 || d.n_q_heads < 1 || d.n_kv_heads < 1 || d.ffn < 1 || d.vocab < 1 || d.max_ctx < 1)
+    return fail(LPS_EINVAL, FN, "shape fields must be positive");
+  if (d.batch < 1 || d.batch > kMaxBatch) return fail(LPS_EINVAL, FN, "batch must be in 1..8");
+  if (d.n_q_heads % d.n_kv_heads) return fail(LPS_EINVAL, FN, "n_q_heads must be a multiple of n_kv_heads");
+  if (!attn_supported(d.head_dim, d.n_q_heads / d.n_kv_heads))
+    return fail(LPS_EINVAL, FN, "head_dim must be 64 or 128 and n_q_heads/n_kv_heads in {1,2,4,8}");
+  const bool int8 = d.weight_dtype == LPS_WEIGHT_INT8_ROWSCALE;
+  const int qw = d.n_q_heads * d.head_dim;
+  if (!gemv_supported(d.n_embd, 2, int8) || !gemv_supported(qw, 1, int8) || !gemv_supported(d.ffn, 1, int8))
+    return fail(LPS_EINVAL, FN, "n_embd, n_q_heads*head_dim and ffn need whole 16-byte weight rows of at most "
+                                "32 KB (16 KB for row pairs)");
+  if (d.n_embd % 4) return fail(LPS_EINVAL, FN, "n_embd must be a multiple of 4");
+  if (!(d.rms_eps > 0.f) || !(d.rope_theta > 0.f)) return fail(LPS_EINVAL, FN, "rms_eps and rope_theta must be > 0");
+  if (!w->layers || !w->out_norm || !w->embed.w || !w->lm_head.w) return fail(LPS_EINVAL, FN, "missing weights");
+
+  lps_model* m = new lps_model();
+  m->d = d;
+  m->int8 = int8;
+  m->single = (d.flags & LPS_FLAG_SINGLE_STREAM) != 0;
+  m->fence = plan->fence;
+  m->N = static_cast<int>(plan->fence.size()) - 1;
+  m->device = rt ? rt->device : 0;
+  if (rt && rt->alloc && !rt->free) {
+    delete m;
+    return fail(LPS_EINVAL, FN, "rt->free is required with rt->alloc");
+  }
+  if (rt) {
+    m->alloc = rt->alloc;
+    m->free_fn = rt->free;
+    m->alloc_ctx = rt->alloc_ctx;
+  }
+  for (int l = 0; l < d.n_layers; ++l) {
+    const lps_layer_weights& L = w->layers[l];
+    if (!L.attn_norm || !L.ffn_norm || !check_matrix(m, L.wq) || !check_matrix(m, L.wk) || !check_matrix(m, L.wv) ||
+        !check_matrix(m, L.wo) || !check_matrix(m, L.w_gate) || !check_matrix(m, L.w_up) ||
+        !check_matrix(m, L.w_down)) {
+      delete m;
+      return fail(LPS_EINVAL, FN, "layer " + std::to_string(l) + " has a missing tensor or scale");
+    }
+  }
+  if (!check_matrix(m, w->embed) || !check_matrix(m, w->lm_head)) {
+    delete m;
+    return fail(LPS_EINVAL, FN, "embed or lm_head is missing its row scales");
+  }
+
+  auto bail = [&](int code, const std::string& why) {
+    release(m);
+    delete m;
+    return fail(code, FN, why);
+  };
+  cudaError_t e = cudaSetDevice(m->device);
+  if (e != cudaSuccess) return bail(LPS_ECUDA, std::string("cudaSetDevice: ") + cudaGetErrorString(e));
+  if (cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) != cudaSuccess)
+    return bail(LPS_ECUDA, "cudaDeviceGetAttribute failed");
+
+  const int N = m->N, B = d.batch, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads, E = d.n_embd;
+  const int half = hd / 2;
+  m->st.resize(N);
+  m->bd.resize(N > 1 ? N - 1 : 0);
+  // streams
+  for (int s = 0; s < N; ++s) {
+    StageDev& S = m->st[s];
+    S.l0 = m->fence[s];
+    S.l1 = m->fence[s + 1];
+    if (rt && rt->streams) {
+      S.stream = static_cast<cudaStream_t>(rt->streams[s]);
+    } else {
+      if (cudaStreamCreateWithFlags(&S.stream, cudaStreamNonBlocking) != cudaSuccess)
+        return bail(LPS_ECUDA, "cudaStreamCreate failed");
+      S.own_stream = true;
+    }
+  }
+  if (rt && rt->streams) {
+    m->rb = static_cast<cudaStream_t>(rt->streams[N]);
+  } else {
+    if (cudaStreamCreateWithFlags(&m->rb, cudaStreamNonBlocking) != cudaSuccess)
+      return bail(LPS_ECUDA, "cudaStreamCreate failed");
+    m->own_rb = true;
+  }
+
+  // chunking of the attention partials, sized for the longest context
+  m->attn_max_chunks = attn_max_chunks(hd, nkv, B, d.max_ctx, m->num_sms);
+
+  // rope table (cos, sin) of angle pos * theta^(-2i/hd), computed in double
+  std::vector<float2> rope(static_cast<size_t>(d.max_ctx) * half);
+  for (int p = 0; p < d.max_ctx; ++p)
+    for (int i = 0; i < half; ++i) {
+      const double ang = static_cast<double>(p) * std::pow(static_cast<double>(d.rope_theta), -2.0 * i / hd);
+      rope[static_cast<size_t>(p) * half + i] = make_float2(static_cast<float>(std::cos(ang)),
+                                                            static_cast<float>(std::sin(ang)));
+    }
+
+  m->status_dev = static_cast<int*>(dev_alloc(m, sizeof(int)));
+  m->status_host = static_cast<int*>(host_alloc(m, sizeof(int)));
+  if (!m->status_dev || !m->status_host) return bail(LPS_ENOMEM, "status word allocation failed");
+  if (cudaMemset(m->status_dev, 0, sizeof(int)) != cudaSuccess) return bail(LPS_ECUDA, "cudaMemset failed");
+
+  const size_t kv_elems = static_cast<size_t>(B) * nkv * d.max_ctx * hd;
+  for (int s = 0; s < N; ++s) {
+    StageDev& S = m->st[s];
+    Uploader up;
+    up.s = S.stream;
+    if (!up.init()) return bail(LPS_ENOMEM, "pinned staging allocation failed");
+    // scratch
+    S.h = static_cast<float*>(dev_alloc(m, sizeof(float) * B * E));
+    S.q = static_cast<float*>(dev_alloc(m, sizeof(float) * B * qw));
+    S.o = static_cast<float*>(dev_alloc(m, sizeof(float) * B * qw));
+    S.a = static_cast<float*>(dev_alloc(m, sizeof(float) * B * d.ffn));
+    S.part = static_cast<float*>(dev_alloc(m, sizeof(float) * B * nq * static_cast<size_t>(m->attn_max_chunks) * (hd + 2)));
+    S.counter = static_cast<int*>(dev_alloc(m, sizeof(int) * B * nkv));
+    S.rope = static_cast<float2*>(dev_alloc(m, sizeof(float2) * rope.size()));
+    if (!S.h || !S.q || !S.o || !S.a || !S.part || !S.counter || !S.rope)
+      return bail(LPS_ENOMEM, "stage " + std::to_string(s) + " scratch allocation failed");
+    if (cudaMemsetAsync(S.counter, 0, sizeof(int) * B * nkv, S.stream) != cudaSuccess ||
+        cudaMemsetAsync(S.h, 0, sizeof(float) * B * E, S.stream) != cudaSuccess)
+      return bail(LPS_ECUDA, "cudaMemsetAsync failed");
+    up.put(S.rope, rope.data(), sizeof(float2) * rope.size());
+
+    // layers owned by this stage
+    S.layers.resize(S.l1 - S.l0);
+    for (int l = S.l0; l < S.l1; ++l) {
+      LayerDev& D = S.layers[l - S.l0];
+      const lps_layer_weights& L = w->layers[l];
+      // W_qkv packed into RoPE pairs: packed unit u = (head hh, i) holds rows
+      // (hh*hd + i, hh*hd + i + hd/2) of [W_q; W_k; W_v]
+      const int rows_qkv = (nq + 2 * nkv) * hd;
+      const size_t rb = static_cast<size_t>(E) * elem_bytes(m);
+      D.w_qkv = dev_alloc(m, rb * rows_qkv);
+      if (!D.w_qkv) return bail(LPS_ENOMEM, "weight allocation failed");
+      std::vector<float> sq(m->int8 ? rows_qkv : 0);
+      for (int r = 0; r < rows_qkv; ++r) {
+        const int u = r >> 1, hh = u / half, i = u % half;
+        const int src = hh * hd + i + ((r & 1) ? half : 0);  // row of the concatenation
+        const lps_matrix* mat;
+        int row;
+        if (src < qw) {
+          mat = &L.wq;
+          row = src;
+        } else if (src < qw + nkv * hd) {
+          mat = &L.wk;
+          row = src - qw;
+        } else {
+          mat = &L.wv;
+          row = src - qw - nkv * hd;
+        }
+        up.put(static_cast<char*>(D.w_qkv) + rb * r, static_cast<const char*>(mat->w) + rb * row, rb);
+        if (m->int8) sq[r] = mat->scale[row];
+      }
+      if (m->int8) {
+        D.s_qkv = static_cast<float*>(dev_alloc(m, sizeof(float) * rows_qkv));
+        if (!D.s_qkv) return bail(LPS_ENOMEM, "scale allocation failed");
+        up.put(D.s_qkv, sq.data(), sizeof(float) * rows_qkv);
+        up.flush();
+      }
+      if (!upload_rows(m, up, L.wo, E, qw, &D.w_o, &D.s_o, [](int r) { return r; }))
+        return bail(LPS_ENOMEM, "W_o upload failed");
+      // gate/up packed as row pairs (gate_i, up_i)
+      {
+        const int rows = 2 * d.ffn;
+        const size_t rbe = static_cast<size_t>(E) * elem_bytes(m);
+        D.w_gu = dev_alloc(m, rbe * rows);
+        if (!D.w_gu) return bail(LPS_ENOMEM, "weight allocation failed");
+        std::vector<float> sg(m->int8 ? rows : 0);
+        for (int r = 0; r < rows; ++r) {
+          const lps_matrix& mat = (r & 1) ? L.w_up : L.w_gate;
+          up.put(static_cast<char*>(D.w_gu) + rbe * r, static_cast<const char*>(mat.w) + rbe * (r >> 1), rbe);
+          if (m->int8) sg[r] = mat.scale[r >> 1];
+        }
+        if (m->int8) {
+          D.s_gu = static_cast<float*>(dev_alloc(m, sizeof(float) * rows));
+          if (!D.s_gu) return bail(LPS_ENOMEM, "scale allocation failed");
+          up.put(D.s_gu, sg.data(), sizeof(float) * rows);
+          up.flush();
+        }
+      }
+      if (!upload_rows(m, up, L.w_down, E, d.ffn, &D.w_d, &D.s_d, [](int r) { return r; }))
+        return bail(LPS_ENOMEM, "W_down upload failed");
+      D.attn_norm = static_cast<float*>(dev_alloc(m, sizeof(float) * E));
+      D.ffn_norm = static_cast<float*>(dev_alloc(m, sizeof(float) * E));
+      D.kc = static_cast<__nv_bfloat16*>(dev_alloc(m, kv_elems * 2));
+      D.vc = static_cast<__nv_bfloat16*>(dev_alloc(m, kv_elems * 2));
+      if (!D.attn_norm || !D.ffn_norm || !D.kc || !D.vc) return bail(LPS_ENOMEM, "KV cache allocation failed");
+      up.put(D.attn_norm, L.attn_norm, sizeof(float) * E);
+      up.put(D.ffn_norm, L.ffn_norm, sizeof(float) * E);
+      if (cudaMemsetAsync(D.kc, 0, kv_elems * 2, S.stream) != cudaSuccess ||
+          cudaMemsetAsync(D.vc, 0, kv_elems * 2, S.stream) != cudaSuccess)
+        return bail(LPS_ECUDA, "cudaMemsetAsync failed");
+      if (d.flags & LPS_FLAG_KEEP_ATTN_OUT) {
+        D.o_keep = static_cast<float*>(dev_alloc(m, sizeof(float) * B * qw));
+        if (!D.o_keep) return bail(LPS_ENOMEM, "attention-output allocation failed");
+      }
+    }
+    if (s == 0) {
+      if (!upload_rows(m, up, w->embed, d.vocab, E, &S.embed, &S.embed_s, [](int r) { return r; }))
+        return bail(LPS_ENOMEM, "embedding upload failed");
+    }
+    if (s == N - 1) {
+      if (!upload_rows(m, up, w->lm_head, d.vocab, E, &S.head, &S.head_s, [](int r) { return r; }))
+        return bail(LPS_ENOMEM, "LM head upload failed");
+      S.out_norm = static_cast<float*>(dev_alloc(m, sizeof(float) * E));
+      if (!S.out_norm) return bail(LPS_ENOMEM, "allocation failed");
+      up.put(S.out_norm, w->out_norm, sizeof(float) * E);
+    }
+    up.flush();
+    if (up.err != cudaSuccess) return bail(LPS_ECUDA, std::string("upload: ") + cudaGetErrorString(up.err));
+    // kernel plans (grid and ring sizing) of this stage's GEMVs
+    S.plan_qkv = gemv_plan((nq + 2 * nkv) * hd, E, 2, int8, m->num_sms);
+    S.plan_o = gemv_plan(E, qw, 1, int8, m->num_sms);
+    S.plan_gu = gemv_plan(2 * d.ffn, E, 2, int8, m->num_sms);
+    S.plan_d = gemv_plan(E, d.ffn, 1, int8, m->num_sms);
+    S.plan_head = gemv_plan(d.vocab, E, 1, int8, m->num_sms);
+    // load barrier: one synchronize per stage (memra_engine::pp, sync_stages_after_load)
+    e = cudaStreamSynchronize(S.stream);
+    if (e != cudaSuccess) return bail(LPS_ECUDA, std::string("load barrier: ") + cudaGetErrorString(e));
+  }
+
+  // boundaries: two persistent slots each, owned by the receiving stage
+  for (int b = 0; b + 1 < N; ++b) {
+    Boundary& Bd = m->bd[b];
+    for (int i = 0; i < 2; ++i) {
+      Bd.slot[i] = static_cast<float*>(dev_alloc(m, sizeof(float) * B * E));
+      if (!Bd.slot[i]) return bail(LPS_ENOMEM, "boundary slot allocation failed");
+      if (cudaMemset(Bd.slot[i], 0, sizeof(float) * B * E) != cudaSuccess ||
+          cudaEventCreateWithFlags(&Bd.ev_tx[i], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&Bd.ev_rx[i], cudaEventDisableTiming) != cudaSuccess)
+        return bail(LPS_ECUDA, "boundary setup failed");
+    }
+  }
+
+  // logits: one eager buffer and the deferred-readback ring
+  const size_t logits_bytes = sizeof(float) * B * static_cast<size_t>(d.vocab);
+  m->eager_logits_dev = static_cast<float*>(dev_alloc(m, logits_bytes));
+  m->eager_host = static_cast<float*>(host_alloc(m, logits_bytes));
+  if (!m->eager_logits_dev || !m->eager_host) return bail(LPS_ENOMEM, "logits allocation failed");
+  const int depth = d.pending_depth > 0 ? d.pending_depth : 4;
+  m->pend.resize(depth);
+  for (auto& p : m->pend) {
+    p.logits_dev = static_cast<float*>(dev_alloc(m, logits_bytes));
+    p.host = static_cast<float*>(host_alloc(m, logits_bytes));
+    p.status_host = static_cast<int*>(host_alloc(m, sizeof(int)));
+    if (!p.logits_dev || !p.host || !p.status_host) return bail(LPS_ENOMEM, "pending slot allocation failed");
+    if (cudaEventCreateWithFlags(&p.ev_done, cudaEventDisableTiming) != cudaSuccess)
+      return bail(LPS_ECUDA, "cudaEventCreate failed");
+  }
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return bail(LPS_ECUDA, std::string("bind: ") + cudaGetErrorString(e));
+  m->filled.assign(B, 0);
+  m->stats.n_stages = N;
+  for (int i = 0; i <= N && i < 17; ++i) m->stats.fence[i] = m->fence[i];
+  *out = m;
+  return LPS_OK;
+}
+
+extern "C" void model_destroy(lps_model* m) {
+  if (!m) return;
+  release(m);
+  delete m;
+}
+
+// ---------------------------------------------------------------------------
+// the step
+// ---------------------------------------------------------------------------
+
+namespace {
+
+int check_step(lps_model* m, const int32_t* tokens, const int32_t* pos, bool tokens_on_host, const char* FN) {
+  if (!m) return fail(LPS_EINVAL, FN, "model is NULL");
+  if (m->failed) return fail(LPS_ECUDA, FN, "model is in a failed state after an earlier device error");
+  if (!tokens || !pos) return fail(LPS_EINVAL, FN, "tokens and pos are required");
+  for (int b = 0; b < m->d.batch; ++b) {
+    if (tokens_on_host && (tokens[b] < 0 || tokens[b] >= m->d.vocab))
+      return fail(LPS_EINVAL, FN, "token " + std::to_string(b) + " out of [0, vocab)");
+    if (pos[b] < 0 || pos[b] >= m->d.max_ctx)
+      return fail(LPS_EINVAL, FN, "pos " + std::to_string(b) + " out of [0, max_ctx)");
+    if (pos[b] > m->filled[b])
+      return fail(LPS_EINVAL, FN, "pos " + std::to_string(b) + " skips unwritten cache rows (pos > filled)");
+  }
+  return LPS_OK;
+}
+
+// Enqueue one step; the last stage writes logits_dev [B][V].
+int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, const int32_t* pos, float* logits_dev,
+                 const char* FN) {
+  const lps_model_desc& d = m->d;
+  const int N = m->N, B = d.batch, E = d.n_embd, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads;
+  const int qw = nq * hd, half = hd / 2;
+  const int par = static_cast<int>(m->step_count & 1);
+  int max_pos = 0;
+  for (int b = 0; b < B; ++b) max_pos = pos[b] > max_pos ? pos[b] : max_pos;
+  const int chunk = attn_chunk(hd, nkv, B, max_pos, m->num_sms);
+  const bool pdl = true;
+  uint64_t launches = 0;
+  cudaEvent_t stop;
+
+#define LAUNCH(kind, stream, call)                                          \
+  do {                                                                      \
+    if (timer_begin(m, kind, stream, &stop)) return fail(LPS_ECUDA, FN, "timer event"); \
+    cudaError_t e_ = (call);                                                \
+    if (e_ != cudaSuccess) {                                                \
+      m->failed = true;                                                     \
+      return cuda_fail(FN, "kernel launch", e_);                            \
+    }                                                                       \
+    timer_end(m, kind, stream, stop);                                       \
+    ++launches;                                                             \
+  } while (0)
+
+  for (int s = 0; s < N; ++s) {
+    StageDev& S = m->st[s];
+    const cudaStream_t cs = m->stream(s);
+    if (!m->single) {
+      if (s > 0) CK(cudaStreamWaitEvent(cs, m->bd[s - 1].ev_tx[par], 0), "wait ev_tx");
+      if (s + 1 < N) CK(cudaStreamWaitEvent(cs, m->bd[s].ev_rx[par], 0), "wait ev_rx");
+    } else if (s > 0) {
+      CK(cudaMemcpyAsync(S.h, m->bd[s - 1].slot[par], sizeof(float) * B * E, cudaMemcpyDeviceToDevice, cs),
+         "boundary copy");
+    }
+    const float* h_first = (s == 0 || m->single) ? S.h : m->bd[s - 1].slot[par];
+    if (s == 0) {
+      EmbedParams ep{};
+      ep.table = S.embed;
+      ep.scale = S.embed_s;
+      ep.tok_dev = tok_dev;
+      for (int b = 0; b < B; ++b) ep.tok[b] = tok_host ? tok_host[b] : 0;
+      ep.d = E;
+      ep.vocab = d.vocab;
+      ep.batch = B;
+      ep.h = S.h;
+      ep.status = m->status_dev;
+      LAUNCH(LPS_KERNEL_EMBED, cs, launch_embed(ep, m->int8, cs, pdl));
+    }
+    for (int l = S.l0; l < S.l1; ++l) {
+      const LayerDev& L = S.layers[l - S.l0];
+      const bool first = (l == S.l0), last = (l == S.l1 - 1);
+      const float* hin = first ? h_first : S.h;
+      float* o_buf = L.o_keep ? L.o_keep : S.o;
+      // RMSNorm -> QKV -> RoPE -> q and KV-cache row pos (per sequence)
+      for (int b = 0; b < B; ++b) {
+        GemvParams p{};
+        p.w = L.w_qkv;
+        p.wscale = L.s_qkv;
+        p.rows = (nq + 2 * nkv) * hd;
+        p.K = E;
+        p.unit_rows = 2;
+        p.units = p.rows / 2;
+        p.units_per_buf = S.plan_qkv.units_per_buf;
+        p.nbuf = S.plan_qkv.nbuf;
+        p.h = hin + static_cast<size_t>(b) * E;
+        p.gain = L.attn_norm;
+        p.eps = d.rms_eps;
+        p.out = S.q + static_cast<size_t>(b) * qw;
+        p.kc = L.kc + static_cast<size_t>(b) * nkv * d.max_ctx * hd;
+        p.vc = L.vc + static_cast<size_t>(b) * nkv * d.max_ctx * hd;
+        p.rope = S.rope + static_cast<size_t>(pos[b]) * half;
+        p.nq = nq;
+        p.nkv = nkv;
+        p.hd = hd;
+        p.max_ctx = d.max_ctx;
+        p.pos = pos[b];
+        p.status = m->status_dev;
+        LAUNCH(LPS_KERNEL_QKV, cs, launch_gemv(p, kEpiQkv, true, m->int8, S.plan_qkv, cs, pdl));
+      }
+      // split-K attention over [0, pos]
+      {
+        AttnParams ap{};
+        ap.q = S.q;
+        ap.kc = L.kc;
+        ap.vc = L.vc;
+        ap.out = o_buf;
+        ap.part = S.part;
+        ap.counter = S.counter;
+        ap.nq = nq;
+        ap.nkv = nkv;
+        ap.hd = hd;
+        ap.max_ctx = d.max_ctx;
+        ap.max_chunks = m->attn_max_chunks;
+        ap.chunk = chunk;
+        for (int b = 0; b < B; ++b) ap.pos[b] = pos[b];
+        ap.scale = 1.0f / std::sqrt(static_cast<float>(hd));
+        ap.status = m->status_dev;
+        LAUNCH(LPS_KERNEL_ATTN, cs, launch_attention(ap, B, max_pos, cs, pdl));
+      }
+      // o-proj + residual (the first layer of a later stage reads the boundary slot)
+      for (int b = 0; b < B; ++b) {
+        GemvParams p{};
+        p.w = L.w_o;
+        p.wscale = L.s_o;
+        p.rows = E;
+        p.K = qw;
+        p.unit_rows = 1;
+        p.units = E;
+        p.units_per_buf = S.plan_o.units_per_buf;
+        p.nbuf = S.plan_o.nbuf;
+        p.x = o_buf + static_cast<size_t>(b) * qw;
+        p.h_in = hin + static_cast<size_t>(b) * E;
+        p.h_out = S.h + static_cast<size_t>(b) * E;
+        p.status = m->status_dev;
+        LAUNCH(LPS_KERNEL_OPROJ, cs, launch_gemv(p, kEpiResidual, false, m->int8, S.plan_o, cs, pdl));
+      }
+      if (first && s > 0 && !m->single) CK(cudaEventRecord(m->bd[s - 1].ev_rx[par], cs), "record ev_rx");
+      // RMSNorm -> gate/up -> SwiGLU
+      for (int b = 0; b < B; ++b) {
+        GemvParams p{};
+        p.w = L.w_gu;
+        p.wscale = L.s_gu;
+        p.rows = 2 * d.ffn;
+        p.K = E;
+        p.unit_rows = 2;
+        p.units = d.ffn;
+        p.units_per_buf = S.plan_gu.units_per_buf;
+        p.nbuf = S.plan_gu.nbuf;
+        p.h = S.h + static_cast<size_t>(b) * E;
+        p.gain = L.ffn_norm;
+        p.eps = d.rms_eps;
+        p.out = S.a + static_cast<size_t>(b) * d.ffn;
+        p.status = m->status_dev;
+        LAUNCH(LPS_KERNEL_GATEUP, cs, launch_gemv(p, kEpiSwiglu, true, m->int8, S.plan_gu, cs, pdl));
+      }
+      // down + residual (the last layer of an earlier stage writes the boundary slot)
+      float* h_out = (last && s + 1 < N && !m->single) ? m->bd[s].slot[par] : S.h;
+      for (int b = 0; b < B; ++b) {
+        GemvParams p{};
+        p.w = L.w_d;
+        p.wscale = L.s_d;
+        p.rows = E;
+        p.K = d.ffn;
+        p.unit_rows = 1;
+        p.units = E;
+        p.units_per_buf = S.plan_d.units_per_buf;
+        p.nbuf = S.plan_d.nbuf;
+        p.x = S.a + static_cast<size_t>(b) * d.ffn;
+        p.h_in = S.h + static_cast<size_t>(b) * E;
+        p.h_out = h_out + static_cast<size_t>(b) * E;
+        p.status = m->status_dev;
+        LAUNCH(LPS_KERNEL_DOWN, cs, launch_gemv(p, kEpiResidual, false, m->int8, S.plan_d, cs, pdl));
+      }
+    }
+    if (s + 1 < N) {
+      if (m->single)
+        CK(cudaMemcpyAsync(m->bd[s].slot[par], S.h, sizeof(float) * B * E, cudaMemcpyDeviceToDevice, cs),
+           "boundary copy");
+      else
+        CK(cudaEventRecord(m->bd[s].ev_tx[par], cs), "record ev_tx");
+      ++m->bd[s].steps;
+      ++m->stats.boundary_crossings;
+    }
+    ++m->stats.stage_walks;
+  }
+  // the last stage: final RMSNorm -> LM head
+  {
+    StageDev& S = m->st[N - 1];
+    const cudaStream_t cs = m->stream(N - 1);
+    for (int b = 0; b < B; ++b) {
+      GemvParams p{};
+      p.w = S.head;
+      p.wscale = S.head_s;
+      p.rows = d.vocab;
+      p.K = E;
+      p.unit_rows = 1;
+      p.units = d.vocab;
+      p.units_per_buf = S.plan_head.units_per_buf;
+      p.nbuf = S.plan_head.nbuf;
+      p.h = S.h + static_cast<size_t>(b) * E;
+      p.gain = S.out_norm;
+      p.eps = d.rms_eps;
+      p.out = logits_dev + static_cast<size_t>(b) * d.vocab;
+      p.status = m->status_dev;
+      LAUNCH(LPS_KERNEL_HEAD, cs, launch_gemv(p, kEpiStore, true, m->int8, S.plan_head, cs, pdl));
+    }
+  }
+#undef LAUNCH
+  for (int b = 0; b < B; ++b) m->filled[b] = pos[b] + 1;
+  ++m->step_count;
+  ++m->stats.steps;
+  m->stats.kernel_launches += launches;
+  return LPS_OK;
+}
+
+int read_status(lps_model* m, int status, const char* FN) {
+  if (status != 0) {
+    m->failed = true;
+    char buf[128];
+    std::snprintf(buf, sizeof buf, "device-side error 0x%x (1: copy wait timed out, 2: buffer wait timed out, "
+                                   "4: drain timed out, 8: bad kernel argument)", status);
+    return fail(LPS_ECUDA, FN, buf);
+  }
+  return LPS_OK;
+}
+
+}  // namespace
+
+extern "C" int decode_step(lps_model* m, const int32_t* tokens, const int32_t* pos, float* logits) {
+  static const char* FN = "decode_step";
+  int rc = check_step(m, tokens, pos, true, FN);
+  if (rc) return rc;
+  if (!logits) return fail(LPS_EINVAL, FN, "logits is NULL");
+  CK(cudaSetDevice(m->device), "cudaSetDevice");
+  rc = enqueue_step(m, tokens, nullptr, pos, m->eager_logits_dev, FN);
+  if (rc) return rc;
+  const cudaStream_t last = m->stream(m->N - 1);
+  const size_t bytes = sizeof(float) * m->d.batch * static_cast<size_t>(m->d.vocab);
+  CK(cudaMemcpyAsync(m->eager_host, m->eager_logits_dev, bytes, cudaMemcpyDeviceToHost, last), "logits copy");
+  CK(cudaMemcpyAsync(m->status_host, m->status_dev, sizeof(int), cudaMemcpyDeviceToHost, last), "status copy");
+  // the last stage's wait chain orders every earlier stage, so this drains the step
+  cudaError_t e = cudaStreamSynchronize(last);
+  if (e != cudaSuccess) {
+    m->failed = true;
+    return cuda_fail(FN, "step", e);
+  }
+  rc = read_status(m, *m->status_host, FN);
+  if (rc) return rc;
+  std::memcpy(logits, m->eager_host, bytes);
+  return LPS_OK;
+}
+
+extern "C" int decode_step_deferred(lps_model* m, const int32_t* tokens, const int32_t* pos, lps_pending** out) {
+  static const char* FN = "decode_step_deferred";
+  if (!out) return fail(LPS_EINVAL, FN, "out is NULL");
+  *out = nullptr;
+  int rc = check_step(m, tokens, pos, true, FN);
+  if (rc) return rc;
+  int slot = -1;
+  for (size_t i = 0; i < m->pend.size(); ++i)
+    if (!m->pend[i].held) {
+      slot = static_cast<int>(i);
+      break;
+    }
+  if (slot < 0) return fail(LPS_EBUSY, FN, "every deferred-readback slot is held; wait and free a pending handle");
+  CK(cudaSetDevice(m->device), "cudaSetDevice");
+  PendingSlot& P = m->pend[slot];
+  rc = enqueue_step(m, tokens, nullptr, pos, P.logits_dev, FN);
+  if (rc) return rc;
+  CK(cudaEventRecord(P.ev_done, m->stream(m->N - 1)), "record completion event");
+  P.held = true;
+  P.drained = false;
+  P.step = m->step_count - 1;
+  ++m->stats.deferred_steps;
+  *out = new lps_pending{m, slot, P.step};
+  return LPS_OK;
+}
+
+extern "C" int pending_wait(lps_pending* p, float* logits, int timeout_ms) {
+  static const char* FN = "pending_wait";
+  if (!p || !logits) return fail(LPS_EINVAL, FN, "pending and logits are required");
+  lps_model* m = p->m;
+  PendingSlot& P = m->pend[p->slot];
+  CK(cudaSetDevice(m->device), "cudaSetDevice");
+  const size_t bytes = sizeof(float) * m->d.batch * static_cast<size_t>(m->d.vocab);
+  if (!P.drained) {
+    if (timeout_ms >= 0) {
+      const auto deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(timeout_ms);
+      for (;;) {
+        const cudaError_t q = cudaEventQuery(P.ev_done);
+        if (q == cudaSuccess) break;
+        if (q != cudaErrorNotReady) {
+          m->failed = true;
+          return cuda_fail(FN, "completion event", q);
+        }
+        if (std::chrono::steady_clock::now() >= deadline)
+          return fail(LPS_ETIMEDOUT, FN, "the step has not completed yet");
+        std::this_thread::sleep_for(std::chrono::microseconds(20));
+      }
+    }
+    // the dedicated readback stream waits the completion event, copies, syncs
+    CK(cudaStreamWaitEvent(m->rb, P.ev_done, 0), "readback wait");
+    CK(cudaMemcpyAsync(P.host, P.logits_dev, bytes, cudaMemcpyDeviceToHost, m->rb), "logits copy");
+    CK(cudaMemcpyAsync(P.status_host, m->status_dev, sizeof(int), cudaMemcpyDeviceToHost, m->rb), "status copy");
+    const cudaError_t e = cudaStreamSynchronize(m->rb);
+    if (e != cudaSuccess) {
+      m->failed = true;
+      return cuda_fail(FN, "readback", e);
+    }
+    P.drained = true;
+    ++m->stats.pending_drains;
+  }
+  const int rc = read_status(m, *P.status_host, FN);
+  if (rc) return rc;
+  std::memcpy(logits, P.host, bytes);
+  return LPS_OK;
+}
+
+extern "C" void pending_free(lps_pending* p) {
+  if (!p) return;
+  p->m->pend[p->slot].held = false;
+  delete p;
+}
+
+extern "C" int decode_step_device(lps_model* m, const int32_t* tokens, const int32_t* pos, float* logits) {
+  static const char* FN = "decode_step_device";
+  int rc = check_step(m, tokens, pos, false, FN);
+  if (rc) return rc;
+  if (!logits) return fail(LPS_EINVAL, FN, "logits is NULL");
+  CK(cudaSetDevice(m->device), "cudaSetDevice");
+  return enqueue_step(m, nullptr, tokens, pos, logits, FN);
+}
+
+extern "C" int model_synchronize(lps_model* m) {
+  static const char* FN = "model_synchronize";
+  if (!m) return fail(LPS_EINVAL, FN, "model is NULL");
+  CK(cudaSetDevice(m->device), "cudaSetDevice");
+  for (int s = 0; s < m->N; ++s) {
+    const cudaError_t e = cudaStreamSynchronize(m->st[s].stream);
+    if (e != cudaSuccess) {
+      m->failed = true;
+      return cuda_fail(FN, "stage stream", e);
+    }
+  }
+  CK(cudaStreamSynchronize(m->rb), "readback stream");
+  CK(cudaMemcpy(m->status_host, m->status_dev, sizeof(int), cudaMemcpyDeviceToHost), "status copy");
+  return read_status(m, *m->status_host, FN);
+}
+
+extern "C" int model_stream(const lps_model* m, int s, void** stream) {
+  static const char* FN = "model_stream";
+  if (!m || !stream || s < 0 || s > m->N) return fail(LPS_EINVAL, FN, "bad argument");
+  *stream = s == m->N ? m->rb : m->stream(s);
+  return LPS_OK;
+}
+
+// ---------------------------------------------------------------------------
+// errors, counters, test hooks
+// ---------------------------------------------------------------------------
+
+extern "C" const char* last_error_string(void) { return g_err.c_str(); }
+
+extern "C" int model_stats(const lps_model* m, lps_stats* out) {
+  if (!m || !out) return fail(LPS_EINVAL, "model_stats", "NULL argument");
+  *out = m->stats;
+  return LPS_OK;
+}
+
+namespace {
+int kv_locate(const lps_model* m, int layer, int b, size_t bytes, const LayerDev** L, cudaStream_t* stream,
+              const char* FN) {
+  if (!m || layer < 0 || layer >= m->d.n_layers || b < 0 || b >= m->d.batch)
+    return fail(LPS_EINVAL, FN, "bad model, layer or sequence");
+  const size_t want = 4ull * m->d.n_kv_heads * m->d.max_ctx * m->d.head_dim;
+  if (bytes != want) return fail(LPS_EINVAL, FN, "bytes must be 4 * nkv * max_ctx * hd");
+  int s = 0;
+  while (layer >= m->fence[s + 1]) ++s;
+  *L = &m->st[s].layers[layer - m->fence[s]];
+  *stream = m->stream(s);
+  return LPS_OK;
+}
+}  // namespace
+
+extern "C" int model_kv_export(const lps_model* m, int layer, int b, void* host, size_t bytes) {
+  static const char* FN = "model_kv_export";
+  const LayerDev* L;
+  cudaStream_t s;
+  int rc = kv_locate(m, layer, b, bytes, &L, &s, FN);
+  if (rc) return rc;
+  if (!host) return fail(LPS_EINVAL, FN, "host is NULL");
+  CK(cudaSetDevice(m->device), "cudaSetDevice");
+  const size_t half = bytes / 2, off = static_cast<size_t>(b) * m->d.n_kv_heads * m->d.max_ctx * m->d.head_dim;
+  CK(cudaStreamSynchronize(s), "stage stream");
+  CK(cudaMemcpy(host, L->kc + off, half, cudaMemcpyDeviceToHost), "K copy");
+  CK(cudaMemcpy(static_cast<char*>(host) + half, L->vc + off, half, cudaMemcpyDeviceToHost), "V copy");
+  return LPS_OK;
+}
+
+extern "C" int model_kv_import(lps_model* m, int layer, int b, const void* host, size_t bytes, int filled) {
+  static const char* FN = "model_kv_import";
+  const LayerDev* L;
+  cudaStream_t s;
+  int rc = kv_locate(m, layer, b, bytes, &L, &s, FN);
+  if (rc) return rc;
+  if (!host || filled < 0 || filled > m->d.max_ctx) return fail(LPS_EINVAL, FN, "bad host buffer or filled");
+  CK(cudaSetDevice(m->device), "cudaSetDevice");
+  const size_t half = bytes / 2, off = static_cast<size_t>(b) * m->d.n_kv_heads * m->d.max_ctx * m->d.head_dim;
+  CK(cudaStreamSynchronize(s), "stage stream");
+  CK(cudaMemcpy(L->kc + off, host, half, cudaMemcpyHostToDevice), "K copy");
+  CK(cudaMemcpy(L->vc + off, static_cast<const char*>(host) + half, half, cudaMemcpyHostToDevice), "V copy");
+  m->filled[b] = filled;
+  return LPS_OK;
+}
+
+extern "C" int model_attn_out(const lps_model* m, int layer, int b, float* host) {
+  static const char* FN = "model_attn_out";
+  if (!m || !host || layer < 0 || layer >= m->d.n_layers || b < 0 || b >= m->d.batch)
+    return fail(LPS_EINVAL, FN, "bad argument");
+  if (!(m->d.flags & LPS_FLAG_KEEP_ATTN_OUT)) return fail(LPS_EINVAL, FN, "bind with LPS_FLAG_KEEP_ATTN_OUT");
+  int s = 0;
+  while (layer >= m->fence[s + 1]) ++s;
+  const LayerDev& L = m->st[s].layers[layer - m->fence[s]];
+  const size_t qw = static_cast<size_t>(m->d.n_q_heads) * m->d.head_dim;
+  CK(cudaSetDevice(m->device), "cudaSetDevice");
+  CK(cudaStreamSynchronize(m->stream(s)), "stage stream");
+  CK(cudaMemcpy(host, L.o_keep + b * qw, qw * sizeof(float), cudaMemcpyDeviceToHost), "copy");
+  return LPS_OK;
+}
+
+extern "C" int model_time_kernel(lps_model* m, int kind, int enable) {
+  if (!m || kind < 0 || kind > LPS_KERNEL_EMBED) return fail(LPS_EINVAL, "model_time_kernel", "bad argument");
+  KTimer& t = m->timers[kind];
+  t.on = enable != 0;
+  t.used = 0;
+  t.total_ms = 0;
+  t.launches = 0;
+  return LPS_OK;
+}
+
+extern "C" int model_kernel_time(lps_model* m, int kind, double* total_ms, uint64_t* launches) {
+  static const char* FN = "model_kernel_time";
+  if (!m || kind < 0 || kind > LPS_KERNEL_EMBED || !total_ms || !launches) return fail(LPS_EINVAL, FN, "bad argument");
+  int rc = model_synchronize(m);
+  if (rc) return rc;
+  KTimer& t = m->timers[kind];
+  for (size_t i = 0; i < t.used; ++i) {
+    float ms = 0.f;
+    CK(cudaEventElapsedTime(&ms, t.ev[i].first, t.ev[i].second), "cudaEventElapsedTime");
+    t.total_ms += ms;
+  }
+  t.used = 0;
+  *total_ms = t.total_ms;
+  *launches = t.launches;
+  return LPS_OK;
+}
