@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fill", default="synthetic", choices=["synthetic", "decode"])
+    ap.add_argument("--serial", action="store_true", help="no overlap between consecutive steps' stages")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="profiling only: keep the first N layers (a smaller case for ncu); not a bench number")
     return ap.parse_args()
 
 
@@ -203,6 +206,9 @@ def main():
     args = parse()
     import synth
     cfg = synth.CONFIGS[args.config]
+    if args.layers:
+        n = min(len(cfg.fence) - 1, args.layers)
+        cfg = cfg.replace(n_layers=args.layers, cuts=tuple(s * args.layers // n for s in range(1, n)))
     ctx = args.ctx if args.ctx is not None else cfg.ctx
     if args.impl == "reference":
         run_reference(args, cfg, ctx)
@@ -230,7 +236,8 @@ def main():
     desc = dict(n_layers=cfg.n_layers, n_embd=cfg.n_embd, n_q_heads=cfg.q_heads, n_kv_heads=cfg.kv_heads,
                 head_dim=cfg.head_dim, ffn=cfg.ffn, vocab=cfg.vocab,
                 weight_dtype=1 if cfg.weight_dtype == "int8" else 0, kv_dtype=0, max_ctx=max_ctx,
-                batch=cfg.batch, pending_depth=4, rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps, flags=0)
+                batch=cfg.batch, pending_depth=4, rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps,
+                flags=lps.LPS_FLAG_SERIAL_STEPS if args.serial else 0)
     plan = lps.stage_plan_create(cfg.n_layers, cuts=list(cfg.cuts))
     model = lps.model_bind(plan, desc, w, device=local)
     B, V = cfg.batch, cfg.vocab
@@ -336,7 +343,8 @@ def main():
         "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": dtype_of(cfg), "data": "synthetic",
         "config": {"workload": wl, "l2": "inputs larger than L2 (every step streams all weights from HBM)",
-                   "cache_fill": args.fill, "parallelism": f"{plan.n_stages} stages on one device"
+                   "cache_fill": args.fill, "steps_overlap": not args.serial,
+                   "parallelism": f"{plan.n_stages} stages on one device"
                    + (f", {n} independent replicas" if n > 1 else "")},
         "hbm_gbs": hbm_gbs, "hbm_frac_of_8tbs": hbm_gbs / NOMINAL_HBM_GBS,
         "hbm_frac_of_measured": hbm_gbs / peaks["hbm_gbs"],

@@ -83,6 +83,11 @@ int stage_of(const lps_stage_plan* plan, int il);
                                       device-to-device copies (memra_engine::pp, pp2_streams_off) */
 #define LPS_FLAG_KEEP_ATTN_OUT 2u  /* keep each layer's attention output of the latest step
                                       readable through model_attn_out (debug) */
+#define LPS_FLAG_SERIAL_STEPS 4u   /* make stage 0 of step t+1 also wait for the last stage of step t.
+                                      By default stages of consecutive steps overlap, bounded
+                                      only by the slot events (tokens t+1.. keep running while
+                                      token t drains: memra_engine::pp, "M2 increment 3"); the
+                                      math is the same either way. */
 
 typedef struct lps_model_desc {
   int n_layers;     /* trunk layers; must equal the plan's */

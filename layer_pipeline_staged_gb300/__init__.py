@@ -14,12 +14,13 @@ gains as f32 vectors. Layout is row-major [out, in].
 from __future__ import annotations
 
 import ctypes
+import gc
 
 import numpy as np
 
 from . import _capi
 from ._capi import (KERNELS, LPS_EBUSY, LPS_ECUDA, LPS_EINVAL, LPS_ENOMEM, LPS_ETIMEDOUT,  # noqa: F401
-                    LPS_FLAG_KEEP_ATTN_OUT, LPS_FLAG_SINGLE_STREAM, LPS_OK)
+                    LPS_FLAG_KEEP_ATTN_OUT, LPS_FLAG_SERIAL_STEPS, LPS_FLAG_SINGLE_STREAM, LPS_OK)
 
 __all__ = ["LpsError", "StagePlan", "Model", "Pending", "stage_plan_create", "stage_plan_from_counts",
            "model_bind", "decode_step", "decode_step_deferred", "pending_wait", "pending_free",
@@ -104,12 +105,18 @@ class _TorchMemory:
         def _alloc(_ctx, nbytes):
             try:
                 return int(torch.cuda.caching_allocator_alloc(int(nbytes), device=device))
-            except Exception:  # out of memory: the library reports LPS_ENOMEM
+            except Exception as e:  # the library then reports LPS_ENOMEM
+                self.last_alloc_error = repr(e)
                 return None
 
         def _free(_ctx, ptr):
-            if ptr:
-                torch.cuda.caching_allocator_delete(int(ptr))
+            try:
+                if ptr:
+                    torch.cuda.caching_allocator_delete(int(ptr))
+            except Exception as e:
+                self.last_alloc_error = repr(e)
+
+        self.last_alloc_error = None
 
         self.alloc = _capi.ALLOC_FN(_alloc)
         self.free = _capi.FREE_FN(_free)
@@ -146,7 +153,18 @@ class Model:
             rt.free = self._mem.free
             rt.streams = ctypes.cast(self._mem.stream_handles, ctypes.POINTER(ctypes.c_void_p))
         h = ctypes.c_void_p()
-        _check(L.model_bind(plan.h, ctypes.byref(self.desc), ctypes.byref(w), ctypes.byref(rt), ctypes.byref(h)))
+        # no garbage collection (and so no other model's destroy) inside the allocator callbacks
+        gc_was_on = gc.isenabled()
+        gc.collect()
+        gc.disable()
+        try:
+            rc = L.model_bind(plan.h, ctypes.byref(self.desc), ctypes.byref(w), ctypes.byref(rt), ctypes.byref(h))
+        finally:
+            if gc_was_on:
+                gc.enable()
+        if rc < 0 and self._mem is not None and self._mem.last_alloc_error:
+            raise LpsError(rc, L.last_error_string().decode() + f" (allocator: {self._mem.last_alloc_error})")
+        _check(rc)
         self.h = h
         self._keep = None
 

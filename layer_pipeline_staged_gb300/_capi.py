@@ -19,6 +19,7 @@ LPS_WEIGHT_INT8_ROWSCALE = 1
 LPS_KV_BF16 = 0
 LPS_FLAG_SINGLE_STREAM = 1
 LPS_FLAG_KEEP_ATTN_OUT = 2
+LPS_FLAG_SERIAL_STEPS = 4
 
 KERNELS = {"qkv": 0, "attn": 1, "oproj": 2, "gateup": 3, "down": 4, "head": 5, "embed": 6}
 

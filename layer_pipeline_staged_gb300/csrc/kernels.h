@@ -2,6 +2,7 @@
 // Shapes are validated by the runtime before any launcher is called.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -41,23 +42,28 @@ struct GemvParams {
   __nv_bfloat16* vc;
   const float2* rope;   // (cos, sin) [hd/2] at this step's position
   int nq, nkv, hd, max_ctx, pos;
+  int nwarps;           // consumer warps (set from the plan at launch)
   int* status;
 };
 
 struct GemvPlan {
-  int grid, smem, units_per_buf, nbuf;
+  int grid, smem, units_per_buf, nbuf, nwarps;
 };
-GemvPlan gemv_plan(int rows, int K, int unit_rows, bool int8, int num_sms);
+GemvPlan gemv_plan(int rows, int K, int unit_rows, bool int8, int num_sms, int max_smem);
+bool gemv_supported(int K, int unit_rows, bool int8, int max_smem);
+void gemv_set_max_smem(int bytes);
 cudaError_t launch_gemv(const GemvParams& p, int epi, bool norm, bool int8, const GemvPlan& plan,
                         cudaStream_t s, bool pdl);
 
 // ---- split-K GQA decode attention -----------------------------------------
 struct AttnParams {
+  CUtensorMap tmap_k;          // this layer's K cache as a 2D bf16 tensor [B*nkv*max_ctx rows][hd],
+  CUtensorMap tmap_v;          // boxes of 64 elements x sub-tile rows, 128-byte swizzle
   const float* q;              // [B][nq*hd]
   const __nv_bfloat16* kc;     // layer base: [B][nkv][max_ctx][hd]
   const __nv_bfloat16* vc;
   float* out;                  // [B][nq*hd]
-  float* part;                 // scratch [B][nq][max_chunks][hd + 2]
+  float* part;                 // scratch [B][nq][max_chunks][hd + 4]: acc, m, l, pad
   int* counter;                // scratch [B][nkv], zero between launches
   int nq, nkv, hd, max_ctx, max_chunks;
   int chunk;                   // positions per CTA (multiple of the sub-tile)

@@ -14,6 +14,8 @@
 // boundary slot and stage s+1's first layer reads it from there); and all
 // shared mutable state of a step is per stage, so stages of consecutive
 // steps can overlap on one device.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <chrono>
@@ -28,7 +30,6 @@
 #include "lps.h"
 
 namespace lps {
-bool gemv_supported(int K, int unit_rows, bool int8);
 bool attn_supported(int hd, int group);
 }  // namespace lps
 
@@ -142,6 +143,7 @@ struct LayerDev {
   __nv_bfloat16* kc = nullptr;  // [B][nkv][max_ctx][hd]
   __nv_bfloat16* vc = nullptr;
   float* o_keep = nullptr;      // [B][nq*hd] with LPS_FLAG_KEEP_ATTN_OUT
+  CUtensorMap tmap_k{}, tmap_v{};  // the caches as 2D TMA tensors (attention sub-tile boxes)
 };
 
 struct StageDev {
@@ -208,6 +210,8 @@ struct lps_model {
   std::vector<Boundary> bd;
   cudaStream_t rb = nullptr;
   bool own_rb = false;
+  bool overlap = true;            // off with LPS_FLAG_SERIAL_STEPS
+  cudaEvent_t ev_step = nullptr;  // recorded by the last stage after each step
   int* status_dev = nullptr;
   int* status_host = nullptr;
   std::vector<int> filled;
@@ -266,6 +270,7 @@ void release(lps_model* m) {
     }
   for (auto& p : m->pend)
     if (p.ev_done) cudaEventDestroy(p.ev_done);
+  if (m->ev_step) cudaEventDestroy(m->ev_step);
   for (auto& t : m->timers)
     for (auto& e : t.ev) {
       cudaEventDestroy(e.first);
@@ -321,10 +326,14 @@ struct Uploader {
     fill = 0;
     dst = nullptr;
   }
-  // Copy `bytes` from host `src` to device `d` (contiguous), through staging.
-  void put(void* d, const void* src, size_t bytes) {
+  // Copy `bytes` from host `src` to device `d`, through staging. Consecutive
+  // puts are merged into one copy only when `same_alloc` says that d continues
+  // the previous put inside the same device allocation (two allocations can be
+  // adjacent in the address space, and one copy must not span both).
+  void put(void* d, const void* src, size_t bytes, bool same_alloc = false) {
     const char* sp = static_cast<const char*>(src);
     char* dp = static_cast<char*>(d);
+    if (!same_alloc) flush();
     while (bytes) {
       if (dst && (dst + fill != dp || fill == kCap)) flush();
       if (!dst) dst = dp;
@@ -343,24 +352,61 @@ size_t elem_bytes(const lps_model* m) { return m->int8 ? 1 : 2; }
 // Upload a [rows, cols] matrix whose device row r comes from host row src_row(r).
 template <class F>
 bool upload_rows(lps_model* m, Uploader& up, const lps_matrix& mat, int rows, int cols, void** w_dev,
-                 float** s_dev, F src_row) {
+                 float** s_dev, F src_row, std::string* why) {
   const size_t rb = static_cast<size_t>(cols) * elem_bytes(m);
   *w_dev = dev_alloc(m, rb * rows);
-  if (!*w_dev) return false;
+  if (!*w_dev) {
+    *why = "device allocation of " + std::to_string(rb * rows) + " bytes failed";
+    return false;
+  }
   const char* src = static_cast<const char*>(mat.w);
-  for (int r = 0; r < rows; ++r) up.put(static_cast<char*>(*w_dev) + rb * r, src + rb * src_row(r), rb);
+  for (int r = 0; r < rows; ++r) up.put(static_cast<char*>(*w_dev) + rb * r, src + rb * src_row(r), rb, r > 0);
   if (m->int8) {
     *s_dev = static_cast<float*>(dev_alloc(m, sizeof(float) * rows));
-    if (!*s_dev) return false;
+    if (!*s_dev) {
+      *why = "device allocation of row scales failed";
+      return false;
+    }
     std::vector<float> s(rows);
     for (int r = 0; r < rows; ++r) s[r] = mat.scale[src_row(r)];
     up.put(*s_dev, s.data(), sizeof(float) * rows);
     up.flush();
   }
+  if (up.err != cudaSuccess) *why = std::string("host-to-device copy: ") + cudaGetErrorString(up.err);
   return up.err == cudaSuccess;
 }
 
 bool check_matrix(const lps_model* m, const lps_matrix& x) { return x.w && (!m->int8 || x.scale); }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+// A cache [rows][hd] bf16 as a 2D tensor read in boxes of 64 elements x box_rows
+// rows with the 128-byte swizzle; rows past the end read as zeros.
+bool make_kv_map(CUtensorMap* map, void* base, int hd, unsigned long long rows, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(hd), rows};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(hd) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 int timer_begin(lps_model* m, int kind, cudaStream_t s, cudaEvent_t* stop) {
   *stop = nullptr;
@@ -405,9 +451,16 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
     return fail(LPS_EINVAL, FN, "head_dim must be 64 or 128 and n_q_heads/n_kv_heads in {1,2,4,8}");
   const bool int8 = d.weight_dtype == LPS_WEIGHT_INT8_ROWSCALE;
   const int qw = d.n_q_heads * d.head_dim;
-  if (!gemv_supported(d.n_embd, 2, int8) || !gemv_supported(qw, 1, int8) || !gemv_supported(d.ffn, 1, int8))
-    return fail(LPS_EINVAL, FN, "n_embd, n_q_heads*head_dim and ffn need whole 16-byte weight rows of at most "
-                                "32 KB (16 KB for row pairs)");
+  const int dev = rt ? rt->device : 0;
+  int max_smem = 0;
+  if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(LPS_ECUDA, FN, "cannot query device " + std::to_string(dev));
+  }
+  if (!gemv_supported(d.n_embd, 2, int8, max_smem) || !gemv_supported(qw, 1, int8, max_smem) ||
+      !gemv_supported(d.ffn, 1, int8, max_smem))
+    return fail(LPS_EINVAL, FN, "n_embd, n_q_heads*head_dim and ffn need whole 16-byte weight rows, and two "
+                                "rows (row pairs) plus the fp32 input vector must fit in shared memory");
   if (d.n_embd % 4) return fail(LPS_EINVAL, FN, "n_embd must be a multiple of 4");
   if (!(d.rms_eps > 0.f) || !(d.rope_theta > 0.f)) return fail(LPS_EINVAL, FN, "rms_eps and rope_theta must be > 0");
   if (!w->layers || !w->out_norm || !w->embed.w || !w->lm_head.w) return fail(LPS_EINVAL, FN, "missing weights");
@@ -416,6 +469,7 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
   m->d = d;
   m->int8 = int8;
   m->single = (d.flags & LPS_FLAG_SINGLE_STREAM) != 0;
+  m->overlap = (d.flags & LPS_FLAG_SERIAL_STEPS) == 0;
   m->fence = plan->fence;
   m->N = static_cast<int>(plan->fence.size()) - 1;
   m->device = rt ? rt->device : 0;
@@ -451,6 +505,7 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
   if (e != cudaSuccess) return bail(LPS_ECUDA, std::string("cudaSetDevice: ") + cudaGetErrorString(e));
   if (cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) != cudaSuccess)
     return bail(LPS_ECUDA, "cudaDeviceGetAttribute failed");
+  gemv_set_max_smem(max_smem);
 
   const int N = m->N, B = d.batch, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads, E = d.n_embd;
   const int half = hd / 2;
@@ -495,6 +550,7 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
   if (cudaMemset(m->status_dev, 0, sizeof(int)) != cudaSuccess) return bail(LPS_ECUDA, "cudaMemset failed");
 
   const size_t kv_elems = static_cast<size_t>(B) * nkv * d.max_ctx * hd;
+  std::string why;
   for (int s = 0; s < N; ++s) {
     StageDev& S = m->st[s];
     Uploader up;
@@ -505,7 +561,7 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
     S.q = static_cast<float*>(dev_alloc(m, sizeof(float) * B * qw));
     S.o = static_cast<float*>(dev_alloc(m, sizeof(float) * B * qw));
     S.a = static_cast<float*>(dev_alloc(m, sizeof(float) * B * d.ffn));
-    S.part = static_cast<float*>(dev_alloc(m, sizeof(float) * B * nq * static_cast<size_t>(m->attn_max_chunks) * (hd + 2)));
+    S.part = static_cast<float*>(dev_alloc(m, sizeof(float) * B * nq * static_cast<size_t>(m->attn_max_chunks) * (hd + 4)));
     S.counter = static_cast<int*>(dev_alloc(m, sizeof(int) * B * nkv));
     S.rope = static_cast<float2*>(dev_alloc(m, sizeof(float2) * rope.size()));
     if (!S.h || !S.q || !S.o || !S.a || !S.part || !S.counter || !S.rope)
@@ -542,7 +598,7 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
           mat = &L.wv;
           row = src - qw - nkv * hd;
         }
-        up.put(static_cast<char*>(D.w_qkv) + rb * r, static_cast<const char*>(mat->w) + rb * row, rb);
+        up.put(static_cast<char*>(D.w_qkv) + rb * r, static_cast<const char*>(mat->w) + rb * row, rb, r > 0);
         if (m->int8) sq[r] = mat->scale[row];
       }
       if (m->int8) {
@@ -551,8 +607,8 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
         up.put(D.s_qkv, sq.data(), sizeof(float) * rows_qkv);
         up.flush();
       }
-      if (!upload_rows(m, up, L.wo, E, qw, &D.w_o, &D.s_o, [](int r) { return r; }))
-        return bail(LPS_ENOMEM, "W_o upload failed");
+      if (!upload_rows(m, up, L.wo, E, qw, &D.w_o, &D.s_o, [](int r) { return r; }, &why))
+        return bail(LPS_ENOMEM, "W_o upload: " + why);
       // gate/up packed as row pairs (gate_i, up_i)
       {
         const int rows = 2 * d.ffn;
@@ -562,7 +618,7 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
         std::vector<float> sg(m->int8 ? rows : 0);
         for (int r = 0; r < rows; ++r) {
           const lps_matrix& mat = (r & 1) ? L.w_up : L.w_gate;
-          up.put(static_cast<char*>(D.w_gu) + rbe * r, static_cast<const char*>(mat.w) + rbe * (r >> 1), rbe);
+          up.put(static_cast<char*>(D.w_gu) + rbe * r, static_cast<const char*>(mat.w) + rbe * (r >> 1), rbe, r > 0);
           if (m->int8) sg[r] = mat.scale[r >> 1];
         }
         if (m->int8) {
@@ -572,13 +628,16 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
           up.flush();
         }
       }
-      if (!upload_rows(m, up, L.w_down, E, d.ffn, &D.w_d, &D.s_d, [](int r) { return r; }))
-        return bail(LPS_ENOMEM, "W_down upload failed");
+      if (!upload_rows(m, up, L.w_down, E, d.ffn, &D.w_d, &D.s_d, [](int r) { return r; }, &why))
+        return bail(LPS_ENOMEM, "W_down upload: " + why);
       D.attn_norm = static_cast<float*>(dev_alloc(m, sizeof(float) * E));
       D.ffn_norm = static_cast<float*>(dev_alloc(m, sizeof(float) * E));
       D.kc = static_cast<__nv_bfloat16*>(dev_alloc(m, kv_elems * 2));
       D.vc = static_cast<__nv_bfloat16*>(dev_alloc(m, kv_elems * 2));
       if (!D.attn_norm || !D.ffn_norm || !D.kc || !D.vc) return bail(LPS_ENOMEM, "KV cache allocation failed");
+      if (!make_kv_map(&D.tmap_k, D.kc, hd, static_cast<unsigned long long>(B) * nkv * d.max_ctx, attn_sub_tile(hd)) ||
+          !make_kv_map(&D.tmap_v, D.vc, hd, static_cast<unsigned long long>(B) * nkv * d.max_ctx, attn_sub_tile(hd)))
+        return bail(LPS_ECUDA, "cuTensorMapEncodeTiled failed for the KV cache");
       up.put(D.attn_norm, L.attn_norm, sizeof(float) * E);
       up.put(D.ffn_norm, L.ffn_norm, sizeof(float) * E);
       if (cudaMemsetAsync(D.kc, 0, kv_elems * 2, S.stream) != cudaSuccess ||
@@ -590,12 +649,12 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
       }
     }
     if (s == 0) {
-      if (!upload_rows(m, up, w->embed, d.vocab, E, &S.embed, &S.embed_s, [](int r) { return r; }))
-        return bail(LPS_ENOMEM, "embedding upload failed");
+      if (!upload_rows(m, up, w->embed, d.vocab, E, &S.embed, &S.embed_s, [](int r) { return r; }, &why))
+        return bail(LPS_ENOMEM, "embedding upload: " + why);
     }
     if (s == N - 1) {
-      if (!upload_rows(m, up, w->lm_head, d.vocab, E, &S.head, &S.head_s, [](int r) { return r; }))
-        return bail(LPS_ENOMEM, "LM head upload failed");
+      if (!upload_rows(m, up, w->lm_head, d.vocab, E, &S.head, &S.head_s, [](int r) { return r; }, &why))
+        return bail(LPS_ENOMEM, "LM head upload: " + why);
       S.out_norm = static_cast<float*>(dev_alloc(m, sizeof(float) * E));
       if (!S.out_norm) return bail(LPS_ENOMEM, "allocation failed");
       up.put(S.out_norm, w->out_norm, sizeof(float) * E);
@@ -603,11 +662,11 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
     up.flush();
     if (up.err != cudaSuccess) return bail(LPS_ECUDA, std::string("upload: ") + cudaGetErrorString(up.err));
     // kernel plans (grid and ring sizing) of this stage's GEMVs
-    S.plan_qkv = gemv_plan((nq + 2 * nkv) * hd, E, 2, int8, m->num_sms);
-    S.plan_o = gemv_plan(E, qw, 1, int8, m->num_sms);
-    S.plan_gu = gemv_plan(2 * d.ffn, E, 2, int8, m->num_sms);
-    S.plan_d = gemv_plan(E, d.ffn, 1, int8, m->num_sms);
-    S.plan_head = gemv_plan(d.vocab, E, 1, int8, m->num_sms);
+    S.plan_qkv = gemv_plan((nq + 2 * nkv) * hd, E, 2, int8, m->num_sms, max_smem);
+    S.plan_o = gemv_plan(E, qw, 1, int8, m->num_sms, max_smem);
+    S.plan_gu = gemv_plan(2 * d.ffn, E, 2, int8, m->num_sms, max_smem);
+    S.plan_d = gemv_plan(E, d.ffn, 1, int8, m->num_sms, max_smem);
+    S.plan_head = gemv_plan(d.vocab, E, 1, int8, m->num_sms, max_smem);
     // load barrier: one synchronize per stage (memra_engine::pp, sync_stages_after_load)
     e = cudaStreamSynchronize(S.stream);
     if (e != cudaSuccess) return bail(LPS_ECUDA, std::string("load barrier: ") + cudaGetErrorString(e));
@@ -625,6 +684,9 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
         return bail(LPS_ECUDA, "boundary setup failed");
     }
   }
+
+  if (cudaEventCreateWithFlags(&m->ev_step, cudaEventDisableTiming) != cudaSuccess)
+    return bail(LPS_ECUDA, "cudaEventCreate failed");
 
   // logits: one eager buffer and the deferred-readback ring
   const size_t logits_bytes = sizeof(float) * B * static_cast<size_t>(d.vocab);
@@ -687,7 +749,10 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
   int max_pos = 0;
   for (int b = 0; b < B; ++b) max_pos = pos[b] > max_pos ? pos[b] : max_pos;
   const int chunk = attn_chunk(hd, nkv, B, max_pos, m->num_sms);
-  const bool pdl = true;
+  // Programmatic dependent launch chains the kernels inside a stage walk; the
+  // first kernel of each walk follows cross-stream event waits and is launched
+  // with full stream ordering instead.
+  bool pdl = false;
   uint64_t launches = 0;
   cudaEvent_t stop;
 
@@ -701,14 +766,17 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
     }                                                                       \
     timer_end(m, kind, stream, stop);                                       \
     ++launches;                                                             \
+    pdl = true;                                                             \
   } while (0)
 
   for (int s = 0; s < N; ++s) {
     StageDev& S = m->st[s];
     const cudaStream_t cs = m->stream(s);
+    pdl = false;
     if (!m->single) {
       if (s > 0) CK(cudaStreamWaitEvent(cs, m->bd[s - 1].ev_tx[par], 0), "wait ev_tx");
       if (s + 1 < N) CK(cudaStreamWaitEvent(cs, m->bd[s].ev_rx[par], 0), "wait ev_rx");
+      if (s == 0 && N > 1 && !m->overlap) CK(cudaStreamWaitEvent(cs, m->ev_step, 0), "wait previous step");
     } else if (s > 0) {
       CK(cudaMemcpyAsync(S.h, m->bd[s - 1].slot[par], sizeof(float) * B * E, cudaMemcpyDeviceToDevice, cs),
          "boundary copy");
@@ -761,6 +829,8 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
       // split-K attention over [0, pos]
       {
         AttnParams ap{};
+        ap.tmap_k = L.tmap_k;
+        ap.tmap_v = L.tmap_v;
         ap.q = S.q;
         ap.kc = L.kc;
         ap.vc = L.vc;
@@ -865,6 +935,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
       p.status = m->status_dev;
       LAUNCH(LPS_KERNEL_HEAD, cs, launch_gemv(p, kEpiStore, true, m->int8, S.plan_head, cs, pdl));
     }
+    if (N > 1 && !m->single && !m->overlap) CK(cudaEventRecord(m->ev_step, cs), "record step event");
   }
 #undef LAUNCH
   for (int b = 0; b < B; ++b) m->filled[b] = pos[b] + 1;

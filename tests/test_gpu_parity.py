@@ -20,6 +20,21 @@ TINY = synth.CONFIGS["tiny"]
 MID = synth.ModelConfig("mid", 95, 2, 512, 32, 8, 128, 512, 1000, "bf16", 1, 0, 0, (1,))
 MID64 = synth.ModelConfig("mid64", 96, 2, 256, 16, 4, 64, 352, 500, "bf16", 2, 0, 0, (1,))
 MID_Q8 = MID.replace(name="mid_q8", index=97, weight_dtype="int8")
+# the 8B-shape layer (n_embd 4096, 32/8 heads of 128, ffn 14336) with a 50k vocabulary: every GEMV
+# streams many ring buffers per CTA, as at full size
+WIDE = synth.ModelConfig("wide", 98, 2, 4096, 32, 8, 128, 14336, 50000, "bf16", 1, 0, 0, (1,))
+WIDE_Q8 = WIDE.replace(name="wide_q8", index=99, weight_dtype="int8")
+
+
+@pytest.mark.parametrize("cfg", [WIDE, WIDE_Q8], ids=lambda c: c.name)
+def test_full_width_layers_match_oracle(cfg):
+    w = synth.make_weights(cfg)
+    T = 6
+    toks = synth.make_tokens(cfg, T)
+    orc = oracle.Oracle(cfg, w, max_ctx=T)
+    m = bind(cfg, w, max_ctx=T)
+    for t in range(T):
+        assert_close(m.decode_step(toks[t], t), orc.step(toks[t], t), cfg, f"step {t}")
 
 
 @pytest.fixture(scope="module")
@@ -101,7 +116,10 @@ def test_kv_rows_match_oracle_and_plans(tiny):
             assert not g[:, T:].any()
             a = synth.bf16_to_f32(g[:, :T]).astype(np.float64)
             b = synth.bf16_to_f32(o[:, :T]).astype(np.float64)
-            assert np.all(np.abs(a - b) <= np.abs(b) * 2 ** -7 + 1e-30)  # at most one bf16 ulp
+            # rows hold the same values up to one bf16 rounding of slightly different fp32/fp64 sums;
+            # near-zero entries carry the sums' absolute error (cancellation), hence the scaled term
+            scale = np.max(np.abs(b), axis=2, keepdims=True)
+            assert np.all(np.abs(a - b) <= np.abs(b) * 2 ** -7 + 1e-4 * scale)
             assert np.mean(a == b) > 0.95
 
 
@@ -149,6 +167,23 @@ def test_attention_long_context_synthetic_cache(cfg, P):
     toks = synth.make_tokens(cfg, 3, seed=77)
     for t in range(3):
         assert_close(m.decode_step(toks[t], P + t), orc.step(toks[t], P + t), cfg, f"P={P} step {t}")
+
+
+@pytest.mark.parametrize("cfg", [MID, MID64], ids=lambda c: c.name)
+def test_attention_very_long_context_combine(cfg):
+    """40k cached rows: hundreds of chunks per (sequence, kv head), so the last
+    CTA merges the partials in several staged pieces."""
+    P = 40000
+    w = synth.make_weights(cfg)
+    max_ctx = P + 2
+    m = bind(cfg, w, max_ctx=max_ctx)
+    orc = oracle.Oracle(cfg, w, max_ctx=max_ctx)
+    for (l, b), (k, v) in random_kv(cfg, 123, cfg.n_layers, max_ctx, P).items():
+        m.kv_import(l, b, k, v, P)
+        orc.kv_import(l, b, k, v, P)
+    toks = synth.make_tokens(cfg, 2, seed=78)
+    for t in range(2):
+        assert_close(m.decode_step(toks[t], P + t), orc.step(toks[t], P + t), cfg, f"step {t}")
 
 
 def test_refusals_leave_state_unchanged(tiny):
@@ -215,3 +250,28 @@ def test_soak_deferred_replays_bit_identical():
             got.append(p.wait())
             p.free()
         assert np.array_equal(np.stack(got), eager), f"replay {rep}"
+
+
+@pytest.mark.parametrize("flags", [0, lps.LPS_FLAG_SERIAL_STEPS], ids=["overlap", "serial"])
+def test_soak_full_width_deferred(flags):
+    """Many pipelined deferred steps at full layer width (four stages, ring
+    wrap-around in every GEMV), stages of consecutive steps overlapping or
+    not: no device-side error, every step equal to the eager run."""
+    cfg = WIDE.replace(n_layers=4, cuts=(1, 2, 3))
+    w = synth.make_weights(cfg)
+    T = 96
+    toks = synth.make_tokens(cfg, T)
+    eager = run_eager(bind(cfg, w, max_ctx=T), toks)
+    m = bind(cfg, w, max_ctx=T, pending_depth=4, flags=flags)
+    pend, got = [], []
+    for t in range(T):
+        pend.append(m.decode_step_deferred(toks[t], t))
+        if len(pend) == 4:
+            p = pend.pop(0)
+            got.append(p.wait())
+            p.free()
+    for p in pend:
+        got.append(p.wait())
+        p.free()
+    m.synchronize()
+    assert np.array_equal(np.stack(got), eager)
