@@ -246,6 +246,35 @@ int model_attn_out(const lps_model* m, int layer, int b, float* host);
 int model_time_kernel(lps_model* m, int kind, int enable);
 int model_kernel_time(lps_model* m, int kind, double* total_ms, uint64_t* launches);
 
+/* ---- allocation-free attention ------------------------------------------ */
+
+/* The paper has no counterpart to this entry point. It serves callers that may
+ * not allocate device memory once they run -- a serving loop with a hard
+ * latency budget (allocation can synchronize the device), or a program whose
+ * GPU memory is handed out once by its own pool. It runs the same split-K GQA
+ * decode attention as the decode step, without a model: its scratch (partial
+ * results and chunk counters) is one file-scope device array of
+ * LPS_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until
+ * exit. It calls no allocator.
+ *   q        device float [batch][n_q_heads * head_dim]
+ *   k_cache  device bf16 [batch][n_kv_heads][max_ctx][head_dim] (one layer),
+ *   v_cache  same layout; 16-byte aligned; rows [0, pos[b]] are read
+ *   out      device float [batch][n_q_heads * head_dim], written
+ *   pos      host int[batch], 0 <= pos[b] < max_ctx
+ *   stream   cudaStream_t to run on (NULL: the default stream)
+ * Runs on the calling thread's current device and returns once enqueued.
+ * The first call on a device looks up the array's address there. All calls
+ * share the array (it keeps the last call's contents; the counters are
+ * cleared by each call): calls that overlap on the GPU race, so keep them in
+ * order on one stream. LPS_EINVAL for unsupported shapes or when the call
+ * would need more scratch than the array holds (message from
+ * attention_decode_noalloc_error()); LPS_ECUDA if a CUDA call fails. */
+#define LPS_NOALLOC_SCRATCH_BYTES (8u << 20)
+int attention_decode_noalloc(const float* q, const void* k_cache, const void* v_cache, float* out, int batch,
+                             int n_q_heads, int n_kv_heads, int head_dim, int max_ctx, const int32_t* pos,
+                             void* stream);
+const char* attention_decode_noalloc_error(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -29,7 +29,7 @@ EXPORTS = (
     "stage_plan_fence", "stage_of", "model_bind", "model_destroy", "decode_step", "decode_step_deferred",
     "pending_wait", "pending_free", "decode_step_device", "model_synchronize", "model_stream",
     "last_error_string", "model_stats", "model_kv_export", "model_kv_import", "model_attn_out",
-    "model_time_kernel", "model_kernel_time",
+    "model_time_kernel", "model_kernel_time", "attention_decode_noalloc", "attention_decode_noalloc_error",
 )
 
 
@@ -105,6 +105,8 @@ def load(path: str = LIB_PATH):
         "model_attn_out": (i, [vp, i, i, vp]),
         "model_time_kernel": (i, [vp, i, i]),
         "model_kernel_time": (i, [vp, i, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_uint64)]),
+        "attention_decode_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, i, vp, vp]),
+        "attention_decode_noalloc_error": (ctypes.c_char_p, []),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
