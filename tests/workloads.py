@@ -43,14 +43,17 @@ def assert_close(got, ref, cfg, what=""):
     return float(e.max())
 
 
-def random_kv(cfg, seed: int, layers: int, max_ctx: int, filled: int):
-    """Synthetic cache rows [0, filled) for every (layer, sequence): uniform bf16 in [-1, 1)."""
-    out = {}
+def iter_random_kv(cfg, seed: int, layers: int, max_ctx: int, filled: int):
+    """Synthetic cache rows [0, filled) for every (layer, sequence): uniform bf16
+    in [-1, 1), yielded one (layer, sequence) at a time."""
     for l in range(layers):
         for b in range(cfg.batch):
             k = synth.uniform_bf16(seed, 2 * (l * cfg.batch + b), (cfg.kv_heads, max_ctx, cfg.head_dim))
             v = synth.uniform_bf16(seed, 2 * (l * cfg.batch + b) + 1, (cfg.kv_heads, max_ctx, cfg.head_dim))
             k[:, filled:] = 0
             v[:, filled:] = 0
-            out[(l, b)] = (k, v)
-    return out
+            yield (l, b), (k, v)
+
+
+def random_kv(cfg, seed: int, layers: int, max_ctx: int, filled: int):
+    return dict(iter_random_kv(cfg, seed, layers, max_ctx, filled))
