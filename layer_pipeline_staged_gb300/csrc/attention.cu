@@ -75,13 +75,21 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "r"(addr));
 }
 
+// c += A.B for one 16-wide k-step: the tensor core sums the 16 exact products
+// from a zero accumulator, then an ordinary (round-to-nearest) fp32 add
+// accumulates, so long sums do not pile up the accumulator's truncation.
 __device__ __forceinline__ void mma_bf16(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                          uint32_t b1) {
+  float d0, d1, d2, d3;
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+      "{%10, %10, %10, %10};"
+      : "=f"(d0), "=f"(d1), "=f"(d2), "=f"(d3)
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+  c[0] += d0;
+  c[1] += d1;
+  c[2] += d2;
+  c[3] += d3;
 }
 
 // Two floats -> a bf16x2 word (low half = first).

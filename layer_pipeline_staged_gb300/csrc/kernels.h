@@ -55,6 +55,43 @@ void gemv_set_max_smem(int bytes);
 cudaError_t launch_gemv(const GemvParams& p, int epi, bool norm, bool int8, const GemvPlan& plan,
                         cudaStream_t s, bool pdl);
 
+// ---- skinny GEMM, batch 2..8, on tensor cores --------------------------------
+// Same epilogues as the GEMV, for all sequences of the batch at once; weights
+// in the tiled layout of skinny_offset().
+struct SkinnyParams {
+  const void* w;           // tiled packed weights
+  const float* wscale;     // int8: per packed row scale
+  int rows, K, KC, KP, units, nbuf, nwarps, batch;  // KP: K padded to whole k-chunks
+  const float* x;          // [B][K]: the input, or h for the fused RMSNorm
+  const float* gain;
+  float eps;
+  float* out;              // q [B][nq*hd] | a [B][ffn] | logits [B][rows] | h_out
+  size_t out_stride;       // per sequence, in floats (also of h_in / h_out)
+  const float* h_in;
+  float* h_out;
+  __nv_bfloat16* kc;       // layer cache [B][nkv][max_ctx][hd]
+  __nv_bfloat16* vc;
+  size_t kv_stride;        // per sequence, in elements
+  const float2* rope;      // the whole (cos, sin) table [max_ctx][hd/2]
+  int nq, nkv, hd, max_ctx;
+  int pos[kMaxBatch];
+  int* status;
+};
+struct SkinnyPlan {
+  int grid, smem, nbuf, nwarps, kc, mt, units;
+  int kp;          // K padded to a whole number of k-chunks (zero columns)
+  int rows_p;      // rows padded to whole units (zero rows)
+};
+SkinnyPlan skinny_plan(int rows, int K, bool int8, int num_sms, int max_smem);
+bool skinny_supported(int rows, int K, bool int8, int num_sms, int max_smem);
+void skinny_set_max_smem(int bytes);
+__host__ __device__ size_t skinny_offset(int r, int k, int K, int kc, int mt, int eb);
+cudaError_t launch_skinny(const SkinnyParams& p, int epi, bool norm, bool int8, const SkinnyPlan& plan,
+                          cudaStream_t s, bool pdl);
+// Rearrange a row-major [rows][K] matrix (elements of eb bytes) into the tiled
+// layout of a [rows_p][kp] zero-padded matrix (dst must be zeroed first).
+cudaError_t launch_retile(const void* src, void* dst, int rows, int K, int kp, int kc, int mt, int eb, cudaStream_t s);
+
 // ---- split-K GQA decode attention -----------------------------------------
 struct AttnParams {
   CUtensorMap tmap_k;          // this layer's K cache as a 2D bf16 tensor [B*nkv*max_ctx rows][hd],

@@ -164,6 +164,7 @@ struct StageDev {
   float* head_s = nullptr;
   float* out_norm = nullptr;
   GemvPlan plan_qkv{}, plan_o{}, plan_gu{}, plan_d{}, plan_head{};
+  SkinnyPlan sk_qkv{}, sk_o{}, sk_gu{}, sk_d{}, sk_head{};  // batch > 1
 };
 
 struct Boundary {
@@ -201,6 +202,7 @@ struct lps_model {
   int num_sms = 0;
   bool int8 = false;
   bool single = false;
+  bool skinny = false;  // batch > 1: tensor-core skinny GEMMs on the tiled weight layout
   lps_alloc_fn alloc = nullptr;
   lps_free_fn free_fn = nullptr;
   void* alloc_ctx = nullptr;
@@ -246,6 +248,18 @@ void* dev_alloc(lps_model* m, size_t bytes) {
   }
   if (p) m->dev_allocs.push_back(p);
   return p;
+}
+
+void dev_free(lps_model* m, void* p) {
+  for (size_t i = 0; i < m->dev_allocs.size(); ++i)
+    if (m->dev_allocs[i] == p) {
+      m->dev_allocs.erase(m->dev_allocs.begin() + static_cast<long>(i));
+      if (m->free_fn)
+        m->free_fn(m->alloc_ctx, p);
+      else
+        cudaFree(p);
+      return;
+    }
 }
 
 void* host_alloc(lps_model* m, size_t bytes) {
@@ -349,27 +363,44 @@ struct Uploader {
 
 size_t elem_bytes(const lps_model* m) { return m->int8 ? 1 : 2; }
 
-// Upload a [rows, cols] matrix whose device row r comes from host row src_row(r).
-template <class F>
-bool upload_rows(lps_model* m, Uploader& up, const lps_matrix& mat, int rows, int cols, void** w_dev,
-                 float** s_dev, F src_row, std::string* why) {
-  const size_t rb = static_cast<size_t>(cols) * elem_bytes(m);
-  *w_dev = dev_alloc(m, rb * rows);
+// Upload a packed [rows, K] matrix: device row r is host row row_ptr(r) (with
+// scale row_scale(r) for int8). Batch 1 keeps it row-major; batch > 1 stores the
+// tiled layout of the skinny GEMM (uploaded row-major into `temp`, then
+// rearranged on the device).
+template <class RowPtr, class RowScale>
+bool place_matrix(lps_model* m, Uploader& up, int rows, int K, RowPtr row_ptr, RowScale row_scale, void** w_dev,
+                  float** s_dev, const SkinnyPlan* sk, void* temp, std::string* why) {
+  const size_t rb = static_cast<size_t>(K) * elem_bytes(m);
+  const size_t bytes = m->skinny ? static_cast<size_t>(sk->rows_p) * sk->kp * elem_bytes(m) : rb * rows;
+  *w_dev = dev_alloc(m, bytes);
   if (!*w_dev) {
-    *why = "device allocation of " + std::to_string(rb * rows) + " bytes failed";
+    *why = "device allocation of " + std::to_string(bytes) + " bytes failed";
     return false;
   }
-  const char* src = static_cast<const char*>(mat.w);
-  for (int r = 0; r < rows; ++r) up.put(static_cast<char*>(*w_dev) + rb * r, src + rb * src_row(r), rb, r > 0);
+  char* dst = static_cast<char*>(m->skinny ? temp : *w_dev);
+  for (int r = 0; r < rows; ++r) up.put(dst + rb * r, row_ptr(r), rb, r > 0);
+  if (m->skinny) {
+    up.flush();
+    cudaError_t e = up.err;
+    if (e == cudaSuccess) e = cudaMemsetAsync(*w_dev, 0, bytes, up.s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(up.s);
+    if (e == cudaSuccess)
+      e = launch_retile(temp, *w_dev, rows, K, sk->kp, sk->kc, sk->mt, static_cast<int>(elem_bytes(m)), up.s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(up.s);
+    if (e != cudaSuccess) {
+      *why = std::string("retiling: ") + cudaGetErrorString(e);
+      return false;
+    }
+  }
   if (m->int8) {
     *s_dev = static_cast<float*>(dev_alloc(m, sizeof(float) * rows));
     if (!*s_dev) {
       *why = "device allocation of row scales failed";
       return false;
     }
-    std::vector<float> s(rows);
-    for (int r = 0; r < rows; ++r) s[r] = mat.scale[src_row(r)];
-    up.put(*s_dev, s.data(), sizeof(float) * rows);
+    std::vector<float> sc(rows);
+    for (int r = 0; r < rows; ++r) sc[r] = row_scale(r);
+    up.put(*s_dev, sc.data(), sizeof(float) * rows);
     up.flush();
   }
   if (up.err != cudaSuccess) *why = std::string("host-to-device copy: ") + cudaGetErrorString(up.err);
@@ -462,6 +493,21 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
     return fail(LPS_EINVAL, FN, "n_embd, n_q_heads*head_dim and ffn need whole 16-byte weight rows, and two "
                                 "rows (row pairs) plus the fp32 input vector must fit in shared memory");
   if (d.n_embd % 4) return fail(LPS_EINVAL, FN, "n_embd must be a multiple of 4");
+  if (d.batch > 1) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(LPS_ECUDA, FN, "cannot query device " + std::to_string(dev));
+    }
+    const int rows_qkv = (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim;
+    if (!skinny_supported(rows_qkv, d.n_embd, int8, sms, max_smem) ||
+        !skinny_supported(d.n_embd, qw, int8, sms, max_smem) ||
+        !skinny_supported(2 * d.ffn, d.n_embd, int8, sms, max_smem) ||
+        !skinny_supported(d.n_embd, d.ffn, int8, sms, max_smem) ||
+        !skinny_supported(d.vocab, d.n_embd, int8, sms, max_smem))
+      return fail(LPS_EINVAL, FN, "batch > 1 needs every projection's rows and columns in multiples of 16 with a "
+                                  "column chunk of 64..1024 dividing them");
+  }
   if (!(d.rms_eps > 0.f) || !(d.rope_theta > 0.f)) return fail(LPS_EINVAL, FN, "rms_eps and rope_theta must be > 0");
   if (!w->layers || !w->out_norm || !w->embed.w || !w->lm_head.w) return fail(LPS_EINVAL, FN, "missing weights");
 
@@ -470,6 +516,7 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
   m->int8 = int8;
   m->single = (d.flags & LPS_FLAG_SINGLE_STREAM) != 0;
   m->overlap = (d.flags & LPS_FLAG_SERIAL_STEPS) == 0;
+  m->skinny = d.batch > 1;
   m->fence = plan->fence;
   m->N = static_cast<int>(plan->fence.size()) - 1;
   m->device = rt ? rt->device : 0;
@@ -506,6 +553,7 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
   if (cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) != cudaSuccess)
     return bail(LPS_ECUDA, "cudaDeviceGetAttribute failed");
   gemv_set_max_smem(max_smem);
+  skinny_set_max_smem(max_smem);
 
   const int N = m->N, B = d.batch, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads, E = d.n_embd;
   const int half = hd / 2;
@@ -551,6 +599,17 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
 
   const size_t kv_elems = static_cast<size_t>(B) * nkv * d.max_ctx * hd;
   std::string why;
+  // batch > 1: a row-major staging buffer on the device for retiling (the largest matrix)
+  void* temp = nullptr;
+  if (m->skinny) {
+    size_t biggest = 0;
+    const size_t sizes[5] = {static_cast<size_t>((nq + 2 * nkv) * hd) * E, static_cast<size_t>(E) * qw,
+                             static_cast<size_t>(2 * d.ffn) * E, static_cast<size_t>(E) * d.ffn,
+                             static_cast<size_t>(d.vocab) * E};
+    for (size_t z : sizes) biggest = z > biggest ? z : biggest;
+    temp = dev_alloc(m, biggest * elem_bytes(m));
+    if (!temp) return bail(LPS_ENOMEM, "retiling buffer allocation failed");
+  }
   for (int s = 0; s < N; ++s) {
     StageDev& S = m->st[s];
     Uploader up;
@@ -571,64 +630,71 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
       return bail(LPS_ECUDA, "cudaMemsetAsync failed");
     up.put(S.rope, rope.data(), sizeof(float2) * rope.size());
 
+    // kernel plans (grid and ring sizing) of this stage's GEMVs
+    const int rows_qkv = (nq + 2 * nkv) * hd;
+    S.plan_qkv = gemv_plan(rows_qkv, E, 2, int8, m->num_sms, max_smem);
+    S.plan_o = gemv_plan(E, qw, 1, int8, m->num_sms, max_smem);
+    S.plan_gu = gemv_plan(2 * d.ffn, E, 2, int8, m->num_sms, max_smem);
+    S.plan_d = gemv_plan(E, d.ffn, 1, int8, m->num_sms, max_smem);
+    S.plan_head = gemv_plan(d.vocab, E, 1, int8, m->num_sms, max_smem);
+    S.sk_qkv = skinny_plan(rows_qkv, E, int8, m->num_sms, max_smem);
+    S.sk_o = skinny_plan(E, qw, int8, m->num_sms, max_smem);
+    S.sk_gu = skinny_plan(2 * d.ffn, E, int8, m->num_sms, max_smem);
+    S.sk_d = skinny_plan(E, d.ffn, int8, m->num_sms, max_smem);
+    S.sk_head = skinny_plan(d.vocab, E, int8, m->num_sms, max_smem);
+
     // layers owned by this stage
     S.layers.resize(S.l1 - S.l0);
+    const size_t rbE = static_cast<size_t>(E) * elem_bytes(m);
     for (int l = S.l0; l < S.l1; ++l) {
       LayerDev& D = S.layers[l - S.l0];
       const lps_layer_weights& L = w->layers[l];
       // W_qkv packed into RoPE pairs: packed unit u = (head hh, i) holds rows
       // (hh*hd + i, hh*hd + i + hd/2) of [W_q; W_k; W_v]
-      const int rows_qkv = (nq + 2 * nkv) * hd;
-      const size_t rb = static_cast<size_t>(E) * elem_bytes(m);
-      D.w_qkv = dev_alloc(m, rb * rows_qkv);
-      if (!D.w_qkv) return bail(LPS_ENOMEM, "weight allocation failed");
-      std::vector<float> sq(m->int8 ? rows_qkv : 0);
-      for (int r = 0; r < rows_qkv; ++r) {
+      auto qkv_src = [&](int r, const lps_matrix** mat) {
         const int u = r >> 1, hh = u / half, i = u % half;
         const int src = hh * hd + i + ((r & 1) ? half : 0);  // row of the concatenation
-        const lps_matrix* mat;
-        int row;
         if (src < qw) {
-          mat = &L.wq;
-          row = src;
-        } else if (src < qw + nkv * hd) {
-          mat = &L.wk;
-          row = src - qw;
-        } else {
-          mat = &L.wv;
-          row = src - qw - nkv * hd;
+          *mat = &L.wq;
+          return src;
         }
-        up.put(static_cast<char*>(D.w_qkv) + rb * r, static_cast<const char*>(mat->w) + rb * row, rb, r > 0);
-        if (m->int8) sq[r] = mat->scale[row];
-      }
-      if (m->int8) {
-        D.s_qkv = static_cast<float*>(dev_alloc(m, sizeof(float) * rows_qkv));
-        if (!D.s_qkv) return bail(LPS_ENOMEM, "scale allocation failed");
-        up.put(D.s_qkv, sq.data(), sizeof(float) * rows_qkv);
-        up.flush();
-      }
-      if (!upload_rows(m, up, L.wo, E, qw, &D.w_o, &D.s_o, [](int r) { return r; }, &why))
+        if (src < qw + nkv * hd) {
+          *mat = &L.wk;
+          return src - qw;
+        }
+        *mat = &L.wv;
+        return src - qw - nkv * hd;
+      };
+      if (!place_matrix(
+              m, up, rows_qkv, E,
+              [&](int r) {
+                const lps_matrix* mat;
+                const int row = qkv_src(r, &mat);
+                return static_cast<const char*>(mat->w) + rbE * row;
+              },
+              [&](int r) {
+                const lps_matrix* mat;
+                const int row = qkv_src(r, &mat);
+                return mat->scale[row];
+              },
+              &D.w_qkv, &D.s_qkv, &S.sk_qkv, temp, &why))
+        return bail(LPS_ENOMEM, "W_qkv upload: " + why);
+      const size_t rbQ = static_cast<size_t>(qw) * elem_bytes(m);
+      if (!place_matrix(
+              m, up, E, qw, [&](int r) { return static_cast<const char*>(L.wo.w) + rbQ * r; },
+              [&](int r) { return L.wo.scale[r]; }, &D.w_o, &D.s_o, &S.sk_o, temp, &why))
         return bail(LPS_ENOMEM, "W_o upload: " + why);
       // gate/up packed as row pairs (gate_i, up_i)
-      {
-        const int rows = 2 * d.ffn;
-        const size_t rbe = static_cast<size_t>(E) * elem_bytes(m);
-        D.w_gu = dev_alloc(m, rbe * rows);
-        if (!D.w_gu) return bail(LPS_ENOMEM, "weight allocation failed");
-        std::vector<float> sg(m->int8 ? rows : 0);
-        for (int r = 0; r < rows; ++r) {
-          const lps_matrix& mat = (r & 1) ? L.w_up : L.w_gate;
-          up.put(static_cast<char*>(D.w_gu) + rbe * r, static_cast<const char*>(mat.w) + rbe * (r >> 1), rbe, r > 0);
-          if (m->int8) sg[r] = mat.scale[r >> 1];
-        }
-        if (m->int8) {
-          D.s_gu = static_cast<float*>(dev_alloc(m, sizeof(float) * rows));
-          if (!D.s_gu) return bail(LPS_ENOMEM, "scale allocation failed");
-          up.put(D.s_gu, sg.data(), sizeof(float) * rows);
-          up.flush();
-        }
-      }
-      if (!upload_rows(m, up, L.w_down, E, d.ffn, &D.w_d, &D.s_d, [](int r) { return r; }, &why))
+      if (!place_matrix(
+              m, up, 2 * d.ffn, E,
+              [&](int r) { return static_cast<const char*>(((r & 1) ? L.w_up : L.w_gate).w) + rbE * (r >> 1); },
+              [&](int r) { return ((r & 1) ? L.w_up : L.w_gate).scale[r >> 1]; }, &D.w_gu, &D.s_gu, &S.sk_gu, temp,
+              &why))
+        return bail(LPS_ENOMEM, "W_gate/W_up upload: " + why);
+      const size_t rbF = static_cast<size_t>(d.ffn) * elem_bytes(m);
+      if (!place_matrix(
+              m, up, E, d.ffn, [&](int r) { return static_cast<const char*>(L.w_down.w) + rbF * r; },
+              [&](int r) { return L.w_down.scale[r]; }, &D.w_d, &D.s_d, &S.sk_d, temp, &why))
         return bail(LPS_ENOMEM, "W_down upload: " + why);
       D.attn_norm = static_cast<float*>(dev_alloc(m, sizeof(float) * E));
       D.ffn_norm = static_cast<float*>(dev_alloc(m, sizeof(float) * E));
@@ -648,12 +714,19 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
         if (!D.o_keep) return bail(LPS_ENOMEM, "attention-output allocation failed");
       }
     }
-    if (s == 0) {
-      if (!upload_rows(m, up, w->embed, d.vocab, E, &S.embed, &S.embed_s, [](int r) { return r; }, &why))
-        return bail(LPS_ENOMEM, "embedding upload: " + why);
+    if (s == 0) {  // the embedding is gathered row by row, so it stays row-major
+      const bool was = m->skinny;
+      m->skinny = false;
+      const bool ok = place_matrix(
+          m, up, d.vocab, E, [&](int r) { return static_cast<const char*>(w->embed.w) + rbE * r; },
+          [&](int r) { return w->embed.scale[r]; }, &S.embed, &S.embed_s, nullptr, nullptr, &why);
+      m->skinny = was;
+      if (!ok) return bail(LPS_ENOMEM, "embedding upload: " + why);
     }
     if (s == N - 1) {
-      if (!upload_rows(m, up, w->lm_head, d.vocab, E, &S.head, &S.head_s, [](int r) { return r; }, &why))
+      if (!place_matrix(
+              m, up, d.vocab, E, [&](int r) { return static_cast<const char*>(w->lm_head.w) + rbE * r; },
+              [&](int r) { return w->lm_head.scale[r]; }, &S.head, &S.head_s, &S.sk_head, temp, &why))
         return bail(LPS_ENOMEM, "LM head upload: " + why);
       S.out_norm = static_cast<float*>(dev_alloc(m, sizeof(float) * E));
       if (!S.out_norm) return bail(LPS_ENOMEM, "allocation failed");
@@ -661,16 +734,12 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
     }
     up.flush();
     if (up.err != cudaSuccess) return bail(LPS_ECUDA, std::string("upload: ") + cudaGetErrorString(up.err));
-    // kernel plans (grid and ring sizing) of this stage's GEMVs
-    S.plan_qkv = gemv_plan((nq + 2 * nkv) * hd, E, 2, int8, m->num_sms, max_smem);
-    S.plan_o = gemv_plan(E, qw, 1, int8, m->num_sms, max_smem);
-    S.plan_gu = gemv_plan(2 * d.ffn, E, 2, int8, m->num_sms, max_smem);
-    S.plan_d = gemv_plan(E, d.ffn, 1, int8, m->num_sms, max_smem);
-    S.plan_head = gemv_plan(d.vocab, E, 1, int8, m->num_sms, max_smem);
     // load barrier: one synchronize per stage (memra_engine::pp, sync_stages_after_load)
     e = cudaStreamSynchronize(S.stream);
     if (e != cudaSuccess) return bail(LPS_ECUDA, std::string("load barrier: ") + cudaGetErrorString(e));
   }
+
+  if (temp) dev_free(m, temp);
 
   // boundaries: two persistent slots each, owned by the receiving stage
   for (int b = 0; b + 1 < N; ++b) {
@@ -739,6 +808,25 @@ int check_step(lps_model* m, const int32_t* tokens, const int32_t* pos, bool tok
   return LPS_OK;
 }
 
+SkinnyParams skinny_params(const lps_model* m, const void* w, const float* wscale, int rows, int K,
+                           const int32_t* pos) {
+  SkinnyParams p{};
+  p.w = w;
+  p.wscale = wscale;
+  p.rows = rows;
+  p.K = K;
+  p.batch = m->d.batch;
+  p.eps = m->d.rms_eps;
+  p.nq = m->d.n_q_heads;
+  p.nkv = m->d.n_kv_heads;
+  p.hd = m->d.head_dim;
+  p.max_ctx = m->d.max_ctx;
+  p.kv_stride = static_cast<size_t>(m->d.n_kv_heads) * m->d.max_ctx * m->d.head_dim;
+  for (int b = 0; b < m->d.batch; ++b) p.pos[b] = pos[b];
+  p.status = m->status_dev;
+  return p;
+}
+
 // Enqueue one step; the last stage writes logits_dev [B][V].
 int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, const int32_t* pos, float* logits_dev,
                  const char* FN) {
@@ -801,7 +889,18 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
       const float* hin = first ? h_first : S.h;
       float* o_buf = L.o_keep ? L.o_keep : S.o;
       // RMSNorm -> QKV -> RoPE -> q and KV-cache row pos (per sequence)
-      for (int b = 0; b < B; ++b) {
+      if (m->skinny) {
+        SkinnyParams p = skinny_params(m, L.w_qkv, L.s_qkv, (nq + 2 * nkv) * hd, E, pos);
+        p.x = hin;
+        p.gain = L.attn_norm;
+        p.out = S.q;
+        p.out_stride = qw;
+        p.kc = L.kc;
+        p.vc = L.vc;
+        p.rope = S.rope;
+        LAUNCH(LPS_KERNEL_QKV, cs, launch_skinny(p, kEpiQkv, true, m->int8, S.sk_qkv, cs, pdl));
+      }
+      for (int b = 0; b < (m->skinny ? 0 : B); ++b) {
         GemvParams p{};
         p.w = L.w_qkv;
         p.wscale = L.s_qkv;
@@ -849,7 +948,15 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
         LAUNCH(LPS_KERNEL_ATTN, cs, launch_attention(ap, B, max_pos, cs, pdl));
       }
       // o-proj + residual (the first layer of a later stage reads the boundary slot)
-      for (int b = 0; b < B; ++b) {
+      if (m->skinny) {
+        SkinnyParams p = skinny_params(m, L.w_o, L.s_o, E, qw, pos);
+        p.x = o_buf;
+        p.h_in = hin;
+        p.h_out = S.h;
+        p.out_stride = E;
+        LAUNCH(LPS_KERNEL_OPROJ, cs, launch_skinny(p, kEpiResidual, false, m->int8, S.sk_o, cs, pdl));
+      }
+      for (int b = 0; b < (m->skinny ? 0 : B); ++b) {
         GemvParams p{};
         p.w = L.w_o;
         p.wscale = L.s_o;
@@ -867,7 +974,15 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
       }
       if (first && s > 0 && !m->single) CK(cudaEventRecord(m->bd[s - 1].ev_rx[par], cs), "record ev_rx");
       // RMSNorm -> gate/up -> SwiGLU
-      for (int b = 0; b < B; ++b) {
+      if (m->skinny) {
+        SkinnyParams p = skinny_params(m, L.w_gu, L.s_gu, 2 * d.ffn, E, pos);
+        p.x = S.h;
+        p.gain = L.ffn_norm;
+        p.out = S.a;
+        p.out_stride = d.ffn;
+        LAUNCH(LPS_KERNEL_GATEUP, cs, launch_skinny(p, kEpiSwiglu, true, m->int8, S.sk_gu, cs, pdl));
+      }
+      for (int b = 0; b < (m->skinny ? 0 : B); ++b) {
         GemvParams p{};
         p.w = L.w_gu;
         p.wscale = L.s_gu;
@@ -886,7 +1001,15 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
       }
       // down + residual (the last layer of an earlier stage writes the boundary slot)
       float* h_out = (last && s + 1 < N && !m->single) ? m->bd[s].slot[par] : S.h;
-      for (int b = 0; b < B; ++b) {
+      if (m->skinny) {
+        SkinnyParams p = skinny_params(m, L.w_d, L.s_d, E, d.ffn, pos);
+        p.x = S.a;
+        p.h_in = S.h;
+        p.h_out = h_out;
+        p.out_stride = E;
+        LAUNCH(LPS_KERNEL_DOWN, cs, launch_skinny(p, kEpiResidual, false, m->int8, S.sk_d, cs, pdl));
+      }
+      for (int b = 0; b < (m->skinny ? 0 : B); ++b) {
         GemvParams p{};
         p.w = L.w_d;
         p.wscale = L.s_d;
@@ -918,7 +1041,15 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
   {
     StageDev& S = m->st[N - 1];
     const cudaStream_t cs = m->stream(N - 1);
-    for (int b = 0; b < B; ++b) {
+    if (m->skinny) {
+      SkinnyParams p = skinny_params(m, S.head, S.head_s, d.vocab, E, pos);
+      p.x = S.h;
+      p.gain = S.out_norm;
+      p.out = logits_dev;
+      p.out_stride = d.vocab;
+      LAUNCH(LPS_KERNEL_HEAD, cs, launch_skinny(p, kEpiStore, true, m->int8, S.sk_head, cs, pdl));
+    }
+    for (int b = 0; b < (m->skinny ? 0 : B); ++b) {
       GemvParams p{};
       p.w = S.head;
       p.wscale = S.head_s;
