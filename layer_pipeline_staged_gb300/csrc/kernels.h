@@ -61,7 +61,7 @@ cudaError_t launch_gemv(const GemvParams& p, int epi, bool norm, bool int8, cons
 struct SkinnyParams {
   const void* w;           // tiled packed weights
   const float* wscale;     // int8: per packed row scale
-  int rows, K, KC, KP, units, nbuf, nwarps, batch;  // KP: K padded to whole k-chunks
+  int rows, K, KC, KP, units, kw, rc, pu, batch;  // KP: K padded to whole k-chunks; see SkinnyPlan
   const float* x;          // [B][K]: the input, or h for the fused RMSNorm
   const float* gain;
   float eps;
@@ -78,19 +78,25 @@ struct SkinnyParams {
   int* status;
 };
 struct SkinnyPlan {
-  int grid, smem, nbuf, nwarps, kc, mt, units;
+  int grid, smem, kc, units;
+  int kw;          // k-groups: warp groups that each own every kw-th k-chunk (1, 2, 4 or 8)
+  int pu;          // units per pass: a CTA's units are taken pu at a time, each pass over all of K
+  int rc;          // k-chunks of a k-group's tiles in flight (its ring holds rc * pu tiles)
+  int upw;         // units per warp in a pass (1, 2, 4 or 8)
   int kp;          // K padded to a whole number of k-chunks (zero columns)
-  int rows_p;      // rows padded to whole units (zero rows)
+  int rows_p;      // rows padded to whole 16-row units (zero rows)
 };
-SkinnyPlan skinny_plan(int rows, int K, bool int8, int num_sms, int max_smem);
-bool skinny_supported(int rows, int K, bool int8, int num_sms, int max_smem);
+SkinnyPlan skinny_plan(int rows, int K, bool int8, int batch, int num_sms, int max_smem);
+// Complete a plan whose grid, units, kc, kw, pu and rc are set; false if it does not fit.
+bool skinny_plan_finish(SkinnyPlan& g, int K, bool int8, int batch, int max_smem);
+bool skinny_supported(int rows, int K, bool int8, int batch, int num_sms, int max_smem);
 void skinny_set_max_smem(int bytes);
-__host__ __device__ size_t skinny_offset(int r, int k, int K, int kc, int mt, int eb);
+__host__ __device__ size_t skinny_offset(int r, int k, int kp, int kc, int units, int grid, int eb);
 cudaError_t launch_skinny(const SkinnyParams& p, int epi, bool norm, bool int8, const SkinnyPlan& plan,
                           cudaStream_t s, bool pdl);
 // Rearrange a row-major [rows][K] matrix (elements of eb bytes) into the tiled
-// layout of a [rows_p][kp] zero-padded matrix (dst must be zeroed first).
-cudaError_t launch_retile(const void* src, void* dst, int rows, int K, int kp, int kc, int mt, int eb, cudaStream_t s);
+// layout of `plan` for a [rows_p][kp] zero-padded matrix (dst must be zeroed first).
+cudaError_t launch_retile(const void* src, void* dst, int rows, int K, const SkinnyPlan& plan, int eb, cudaStream_t s);
 
 // ---- split-K GQA decode attention -----------------------------------------
 struct AttnParams {

@@ -385,7 +385,7 @@ bool place_matrix(lps_model* m, Uploader& up, int rows, int K, RowPtr row_ptr, R
     if (e == cudaSuccess) e = cudaMemsetAsync(*w_dev, 0, bytes, up.s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(up.s);
     if (e == cudaSuccess)
-      e = launch_retile(temp, *w_dev, rows, K, sk->kp, sk->kc, sk->mt, static_cast<int>(elem_bytes(m)), up.s);
+      e = launch_retile(temp, *w_dev, rows, K, *sk, static_cast<int>(elem_bytes(m)), up.s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(up.s);
     if (e != cudaSuccess) {
       *why = std::string("retiling: ") + cudaGetErrorString(e);
@@ -500,13 +500,13 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
       return fail(LPS_ECUDA, FN, "cannot query device " + std::to_string(dev));
     }
     const int rows_qkv = (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim;
-    if (!skinny_supported(rows_qkv, d.n_embd, int8, sms, max_smem) ||
-        !skinny_supported(d.n_embd, qw, int8, sms, max_smem) ||
-        !skinny_supported(2 * d.ffn, d.n_embd, int8, sms, max_smem) ||
-        !skinny_supported(d.n_embd, d.ffn, int8, sms, max_smem) ||
-        !skinny_supported(d.vocab, d.n_embd, int8, sms, max_smem))
-      return fail(LPS_EINVAL, FN, "batch > 1 needs every projection's rows and columns in multiples of 16 with a "
-                                  "column chunk of 64..1024 dividing them");
+    if (!skinny_supported(rows_qkv, d.n_embd, int8, d.batch, sms, max_smem) ||
+        !skinny_supported(d.n_embd, qw, int8, d.batch, sms, max_smem) ||
+        !skinny_supported(2 * d.ffn, d.n_embd, int8, d.batch, sms, max_smem) ||
+        !skinny_supported(d.n_embd, d.ffn, int8, d.batch, sms, max_smem) ||
+        !skinny_supported(d.vocab, d.n_embd, int8, d.batch, sms, max_smem))
+      return fail(LPS_EINVAL, FN, "batch > 1 needs every projection's columns in multiples of 16, rows even and "
+                                  "at most 64 16-row units (1024 rows) per SM");
   }
   if (!(d.rms_eps > 0.f) || !(d.rope_theta > 0.f)) return fail(LPS_EINVAL, FN, "rms_eps and rope_theta must be > 0");
   if (!w->layers || !w->out_norm || !w->embed.w || !w->lm_head.w) return fail(LPS_EINVAL, FN, "missing weights");
@@ -637,11 +637,11 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
     S.plan_gu = gemv_plan(2 * d.ffn, E, 2, int8, m->num_sms, max_smem);
     S.plan_d = gemv_plan(E, d.ffn, 1, int8, m->num_sms, max_smem);
     S.plan_head = gemv_plan(d.vocab, E, 1, int8, m->num_sms, max_smem);
-    S.sk_qkv = skinny_plan(rows_qkv, E, int8, m->num_sms, max_smem);
-    S.sk_o = skinny_plan(E, qw, int8, m->num_sms, max_smem);
-    S.sk_gu = skinny_plan(2 * d.ffn, E, int8, m->num_sms, max_smem);
-    S.sk_d = skinny_plan(E, d.ffn, int8, m->num_sms, max_smem);
-    S.sk_head = skinny_plan(d.vocab, E, int8, m->num_sms, max_smem);
+    S.sk_qkv = skinny_plan(rows_qkv, E, int8, B, m->num_sms, max_smem);
+    S.sk_o = skinny_plan(E, qw, int8, B, m->num_sms, max_smem);
+    S.sk_gu = skinny_plan(2 * d.ffn, E, int8, B, m->num_sms, max_smem);
+    S.sk_d = skinny_plan(E, d.ffn, int8, B, m->num_sms, max_smem);
+    S.sk_head = skinny_plan(d.vocab, E, int8, B, m->num_sms, max_smem);
 
     // layers owned by this stage
     S.layers.resize(S.l1 - S.l0);
