@@ -201,6 +201,13 @@ int decode_step_device(lps_model* m, const int32_t* tokens, const int32_t* pos, 
 /* Block until every stream of the model is idle; reports device-side errors. */
 int model_synchronize(lps_model* m);
 
+/* Switch step overlap off (serial = 1: stage 0 of a step waits for the last
+ * stage of the previous step, as LPS_FLAG_SERIAL_STEPS does at bind time) or
+ * back on (serial = 0). Synchronizes the model first; results are unchanged
+ * (each stage's kernels run in the same order either way). Used to time a
+ * kernel family without other stages' kernels running beside it. */
+int model_set_serial_steps(lps_model* m, int serial);
+
 /* The cudaStream_t of stage s (0..N-1) or of the readback stream (s = N). */
 int model_stream(const lps_model* m, int s, void** stream);
 
@@ -274,6 +281,12 @@ int attention_decode_noalloc(const float* q, const void* k_cache, const void* v_
                              int n_q_heads, int n_kv_heads, int head_dim, int max_ctx, const int32_t* pos,
                              void* stream);
 const char* attention_decode_noalloc_error(void);
+
+/* The scratch bytes attention_decode_noalloc needs for these shapes on the
+ * current device (the call is refused when they exceed
+ * LPS_NOALLOC_SCRATCH_BYTES), or -1 for unsupported shapes or without a
+ * device. Launches nothing. */
+long long attention_decode_noalloc_scratch_bytes(int batch, int n_q_heads, int n_kv_heads, int head_dim, int max_pos);
 
 #ifdef __cplusplus
 }

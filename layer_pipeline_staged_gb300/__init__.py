@@ -20,7 +20,8 @@ import numpy as np
 
 from . import _capi
 from ._capi import (KERNELS, LPS_EBUSY, LPS_ECUDA, LPS_EINVAL, LPS_ENOMEM, LPS_ETIMEDOUT,  # noqa: F401
-                    LPS_FLAG_KEEP_ATTN_OUT, LPS_FLAG_SERIAL_STEPS, LPS_FLAG_SINGLE_STREAM, LPS_OK)
+                    LPS_FLAG_KEEP_ATTN_OUT, LPS_FLAG_SERIAL_STEPS, LPS_FLAG_SINGLE_STREAM, LPS_NOALLOC_SCRATCH_BYTES,
+                    LPS_OK)
 
 __all__ = ["LpsError", "StagePlan", "Model", "Pending", "stage_plan_create", "stage_plan_from_counts",
            "model_bind", "decode_step", "decode_step_deferred", "pending_wait", "pending_free",
@@ -225,6 +226,9 @@ class Model:
         out = np.empty((self.desc.n_q_heads, self.desc.head_dim), np.float32)
         _check(load().model_attn_out(self.h, layer, b, _ptr(out)))
         return out
+
+    def set_serial_steps(self, serial: bool):
+        _check(load().model_set_serial_steps(self.h, int(serial)))
 
     def time_kernel(self, kind: str, enable: bool = True):
         _check(load().model_time_kernel(self.h, KERNELS[kind], int(enable)))

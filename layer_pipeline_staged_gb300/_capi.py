@@ -17,6 +17,7 @@ LPS_EBUSY = -5
 LPS_WEIGHT_BF16 = 0
 LPS_WEIGHT_INT8_ROWSCALE = 1
 LPS_KV_BF16 = 0
+LPS_NOALLOC_SCRATCH_BYTES = 8 << 20
 LPS_FLAG_SINGLE_STREAM = 1
 LPS_FLAG_KEEP_ATTN_OUT = 2
 LPS_FLAG_SERIAL_STEPS = 4
@@ -29,7 +30,8 @@ EXPORTS = (
     "stage_plan_fence", "stage_of", "model_bind", "model_destroy", "decode_step", "decode_step_deferred",
     "pending_wait", "pending_free", "decode_step_device", "model_synchronize", "model_stream",
     "last_error_string", "model_stats", "model_kv_export", "model_kv_import", "model_attn_out",
-    "model_time_kernel", "model_kernel_time", "attention_decode_noalloc", "attention_decode_noalloc_error",
+    "model_time_kernel", "model_kernel_time", "model_set_serial_steps", "attention_decode_noalloc", "attention_decode_noalloc_error",
+    "attention_decode_noalloc_scratch_bytes",
 )
 
 
@@ -104,9 +106,11 @@ def load(path: str = LIB_PATH):
         "model_kv_import": (i, [vp, i, i, vp, ctypes.c_size_t, i]),
         "model_attn_out": (i, [vp, i, i, vp]),
         "model_time_kernel": (i, [vp, i, i]),
+        "model_set_serial_steps": (i, [vp, i]),
         "model_kernel_time": (i, [vp, i, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_uint64)]),
         "attention_decode_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, i, vp, vp]),
         "attention_decode_noalloc_error": (ctypes.c_char_p, []),
+        "attention_decode_noalloc_scratch_bytes": (ctypes.c_longlong, [i, i, i, i, i]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)

@@ -16,7 +16,9 @@
 //     wrote them), the one holding row pos after it (the QKV kernel just wrote
 //     that row);
 //   - the dot products run on tensor cores (mma.sync m16n8k16, bf16 in, fp32
-//     accumulate). Row 2h of the 16-row operand is bf16(q_h) and row 2h+1 is
+//     accumulate; a score's HD/16 k-steps accumulate on the tensor core, the
+//     P.V sums over the context add each k-step's MMA with a round-to-nearest
+//     fp32 add). Row 2h of the 16-row operand is bf16(q_h) and row 2h+1 is
 //     bf16(q_h - bf16(q_h)), so q keeps about 16 significant bits; the
 //     probabilities are split the same way for P.V;
 //   - each warp owns a 16-position slice of every sub-tile and keeps its own
@@ -77,12 +79,12 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
 
 // c += A.B for one 16-wide k-step: the tensor core sums the 16 exact products
 // from a zero accumulator, then an ordinary (round-to-nearest) fp32 add
-// accumulates, so long sums do not pile up the accumulator's truncation.
+// accumulates, so long sums (P.V over the whole context) do not pile up the
+// accumulator's truncation. Not volatile: independent MMAs may overlap.
 __device__ __forceinline__ void mma_bf16(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                          uint32_t b1) {
   float d0, d1, d2, d3;
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%10, %10, %10, %10};"
       : "=f"(d0), "=f"(d1), "=f"(d2), "=f"(d3)
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
@@ -90,6 +92,16 @@ __device__ __forceinline__ void mma_bf16(float* c, uint32_t a0, uint32_t a1, uin
   c[1] += d1;
   c[2] += d2;
   c[3] += d3;
+}
+
+// c += A.B accumulated on the tensor core, for short sums (a score's HD/16
+// k-steps, started from zero for every sub-tile).
+__device__ __forceinline__ void mma_bf16_acc(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                             uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // Two floats -> a bf16x2 word (low half = first).
@@ -214,8 +226,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const __grid_constant
           const uint32_t addr = kbase + part * S::BOX + swz(r, ch + (mtx & 1));
           uint32_t b0, b1, b2, b3;
           ldsm_x4(addr, b0, b1, b2, b3);
-          mma_bf16(sc[nt], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-          mma_bf16(sc[nt + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+          mma_bf16_acc(sc[nt], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+          mma_bf16_acc(sc[nt + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
         }
       }
       // combine the hi and lo rows of each head, scale, mask, update the running max
@@ -366,10 +378,13 @@ __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const __grid_constant
       Ls[tid] = 0.f;
     }
     const float* gbase = p.part + (static_cast<size_t>(b) * p.nq + g * G) * p.max_chunks * stride;
+    const bool one_piece = nchunks <= cap;  // then both passes use one staged copy
+    int loads = 0;
     for (int pass = 0; pass < 2; ++pass) {
       for (int c0 = 0; c0 < nchunks; c0 += cap) {
         const int nc = min(cap, nchunks - c0);
         __syncthreads();  // the staging area is free
+        if (one_piece && pass == 1) goto staged;
         if (tid == 0) {
           const uint32_t bytes = static_cast<uint32_t>(nc) * stride * 4;
           mbar_arrive_expect_tx(&sm.full[0], G * bytes);
@@ -377,12 +392,15 @@ __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const __grid_constant
             bulk_g2s_plain(buf + hh * nc * stride, gbase + (static_cast<size_t>(hh) * p.max_chunks + c0) * stride,
                            bytes, &sm.full[0]);
         }
-        // phases of full[0] continue from the ring's count
-        const int phase = (nsub + kRing - 1) / kRing + pass * ((nchunks + cap - 1) / cap) + c0 / cap;
-        if (!mbar_wait(&sm.full[0], phase & 1)) {
-          if (tid == 0) report_error(p.status, kErrWaitFull | (6 << 8));
-          return;
+        {
+          // phases of full[0] continue from the ring's count
+          const int phase = (nsub + kRing - 1) / kRing + loads++;
+          if (!mbar_wait(&sm.full[0], phase & 1)) {
+            if (tid == 0) report_error(p.status, kErrWaitFull | (6 << 8));
+            return;
+          }
         }
+      staged:
         if (pass == 0) {
           for (int hh = warp; hh < G; hh += kWarps) {
             float mx = -INFINITY;
@@ -467,21 +485,29 @@ cudaError_t launch_h(const AttnParams& p, int batch, int max_pos, cudaStream_t s
 
 int attn_sub_tile(int hd) { return 8192 / hd; }
 
-// Positions per CTA, a multiple of 16: about two resident CTAs per SM per
-// wave, with up to eight waves when the cache is long, so that the CTAs split
-// the cached bytes evenly over the SMs.
+// Positions per CTA: a whole number cs of sub-tiles, chosen for the shortest
+// modelled time: waves of two resident CTAs per SM, each wave as long as cs
+// sub-tiles plus a fixed per-CTA cost (start-up, first copy, partial write)
+// of about two sub-tiles; ties go to the longer chunk (fewer partials to
+// combine). Every CTA of a wave streams at about the same rate, so the cached
+// bytes spread evenly over the SMs without a ragged last wave.
 int attn_chunk(int hd, int nkv, int batch, int max_pos, int num_sms) {
-  const int n = max_pos + 1;
-  const int groups = nkv * batch;
-  const int slots = 2 * num_sms;
-  const long long nsub_total = static_cast<long long>(groups) * ((n + attn_sub_tile(hd) - 1) / attn_sub_tile(hd));
-  long long waves = nsub_total / (2LL * slots);
-  waves = waves < 1 ? 1 : (waves > 8 ? 8 : waves);
-  int per_group = static_cast<int>((waves * slots + groups - 1) / groups);
-  per_group = per_group < 1 ? 1 : per_group;
-  int chunk = (n + per_group - 1) / per_group;
-  chunk = (chunk + 15) / 16 * 16;
-  return chunk;
+  constexpr long long kOverhead = 2;
+  const int ts = attn_sub_tile(hd);
+  const int nsub = (max_pos + 1 + ts - 1) / ts;  // sub-tiles of one (sequence, kv head)
+  const long long groups = static_cast<long long>(nkv) * batch;
+  const long long slots = 2LL * num_sms;
+  long long best = -1;
+  int best_cs = nsub;
+  for (int cs = 1; cs <= nsub; ++cs) {
+    const long long ctas = groups * ((nsub + cs - 1) / cs);
+    const long long cost = (ctas + slots - 1) / slots * (cs + kOverhead);
+    if (best < 0 || cost <= best) {
+      best = cost;
+      best_cs = cs;
+    }
+  }
+  return best_cs * ts;
 }
 
 int attn_max_chunks(int hd, int nkv, int batch, int max_ctx, int num_sms) {

@@ -98,6 +98,33 @@ bool encode_cache(CUtensorMap* map, const void* base, int hd, unsigned long long
 
 extern "C" const char* attention_decode_noalloc_error(void) { return g_err.c_str(); }
 
+namespace {
+// Scratch of one call: the counters (rounded up to 256 bytes) and the partials.
+void scratch_need(int batch, int n_q_heads, int n_kv_heads, int head_dim, int nchunks, size_t* counter_bytes,
+                  size_t* part_bytes) {
+  *counter_bytes = (static_cast<size_t>(batch) * n_kv_heads * sizeof(int) + 255) / 256 * 256;
+  *part_bytes = static_cast<size_t>(batch) * n_q_heads * nchunks * (head_dim + 4) * sizeof(float);
+}
+}  // namespace
+
+extern "C" long long attention_decode_noalloc_scratch_bytes(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                                            int max_pos) {
+  using namespace lps;
+  if (batch < 1 || batch > kMaxBatch || n_kv_heads < 1 || n_q_heads % n_kv_heads ||
+      !attn_supported(head_dim, n_q_heads / n_kv_heads) || max_pos < 0)
+    return -1;
+  int dev = 0, num_sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                 cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  const int chunk = attn_chunk(head_dim, n_kv_heads, batch, max_pos, num_sms);
+  size_t counter_bytes = 0, part_bytes = 0;
+  scratch_need(batch, n_q_heads, n_kv_heads, head_dim, (max_pos + 1 + chunk - 1) / chunk, &counter_bytes, &part_bytes);
+  return static_cast<long long>(counter_bytes + part_bytes);
+}
+
 extern "C" int attention_decode_noalloc(const float* q, const void* k_cache, const void* v_cache, float* out,
                                         int batch, int n_q_heads, int n_kv_heads, int head_dim, int max_ctx,
                                         const int32_t* pos, void* stream) {
@@ -126,8 +153,8 @@ extern "C" int attention_decode_noalloc(const float* q, const void* k_cache, con
   // [B][nq][nchunks][hd + 4] floats
   const int chunk = attn_chunk(head_dim, n_kv_heads, batch, max_pos, num_sms);
   const int nchunks = (max_pos + 1 + chunk - 1) / chunk;
-  const size_t counter_bytes = (static_cast<size_t>(batch) * n_kv_heads * sizeof(int) + 255) / 256 * 256;
-  const size_t part_bytes = static_cast<size_t>(batch) * n_q_heads * nchunks * (head_dim + 4) * sizeof(float);
+  size_t counter_bytes = 0, part_bytes = 0;
+  scratch_need(batch, n_q_heads, n_kv_heads, head_dim, nchunks, &counter_bytes, &part_bytes);
   if (counter_bytes + part_bytes > kScratchBytes)
     return fail(LPS_EINVAL, "needs " + std::to_string(counter_bytes + part_bytes) + " bytes of scratch, more than the " +
                                 std::to_string(kScratchBytes) + " this entry point holds; use fewer sequences or "

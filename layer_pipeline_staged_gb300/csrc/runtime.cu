@@ -1290,6 +1290,14 @@ extern "C" int model_attn_out(const lps_model* m, int layer, int b, float* host)
   return LPS_OK;
 }
 
+extern "C" int model_set_serial_steps(lps_model* m, int serial) {
+  if (!m) return fail(LPS_EINVAL, "model_set_serial_steps", "model is NULL");
+  const int rc = model_synchronize(m);
+  if (rc) return rc;
+  m->overlap = serial == 0;
+  return LPS_OK;
+}
+
 extern "C" int model_time_kernel(lps_model* m, int kind, int enable) {
   if (!m || kind < 0 || kind > LPS_KERNEL_EMBED) return fail(LPS_EINVAL, "model_time_kernel", "bad argument");
   KTimer& t = m->timers[kind];

@@ -23,7 +23,7 @@ def _declared():
     src = open(os.path.join(ROOT, "include", "lps.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     lines = [ln for ln in src.splitlines() if not ln.lstrip().startswith("typedef")]
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", "\n".join(lines), flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?(?:long\s+)?\w+\s*\*?\s*(\w+)\s*\(", "\n".join(lines), flags=re.M)))
 
 
 def test_exports_every_declared_symbol():

@@ -76,8 +76,23 @@ def test_noalloc_attention_matches_decode_step():
 
 
 def test_noalloc_refuses_oversized_calls():
+    """A call whose partials do not fit the static scratch is refused before
+    any launch. The buffers are real and sized for the call, and the library's
+    own requirement for these shapes is checked to exceed the scratch first, so
+    the call is never made with shapes the entry point would accept."""
+    import torch
+
+    B, nq, nkv, hd, max_ctx, P = 8, 8192, 1024, 128, 2, 1
     L = _capi.load()
-    pos = (ctypes.c_int32 * 8)(*([2_000_000] * 8))
-    rc = L.attention_decode_noalloc(16, 16, 16, 16, 8, 8, 1, 128, 2_000_001, pos, None)
+    need = L.attention_decode_noalloc_scratch_bytes(B, nq, nkv, hd, P)
+    assert need > lps.LPS_NOALLOC_SCRATCH_BYTES, f"shapes need only {need} bytes: not an oversized call"
+    q = torch.zeros(B, nq * hd, device="cuda")
+    out = torch.zeros(B, nq * hd, device="cuda")
+    k = torch.zeros(B * nkv * max_ctx * hd, dtype=torch.int16, device="cuda")
+    v = torch.zeros(B * nkv * max_ctx * hd, dtype=torch.int16, device="cuda")
+    pos = (ctypes.c_int32 * B)(*([P] * B))
+    rc = L.attention_decode_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, nq, nkv, hd, max_ctx,
+                                    pos, torch.cuda.current_stream().cuda_stream)
     assert rc == lps.LPS_EINVAL
     assert "scratch" in L.attention_decode_noalloc_error().decode()
+    torch.cuda.synchronize()
