@@ -97,18 +97,20 @@ def dominant_kernel(cfg, pos: int) -> str:
     return max(("gateup", "attn"), key=lambda k: kernel_bytes(cfg, k, pos))
 
 
-def kernel_traffic(kind: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it still matches the kernel source."""
+def kernel_traffic(kind: str, cfg_name: str):
+    """DRAM bytes per launch of a kernel family on a workload, from the committed ncu
+    summary, if the kernel's sources still match the ones it was captured with."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
-        data = json.load(open(path))
+        ent = json.load(open(path))["entries"].get(f"{kind}:{cfg_name}")
     except Exception:
         return None
-    ent = data.get(kind)
-    if not ent or ent.get("workload") != workload:
+    if not ent:
         return None
-    src = open(os.path.join(ROOT, "layer_pipeline_staged_gb300", "csrc", ent["source"]), "rb").read()
-    if hashlib.sha256(src).hexdigest()[:16] != ent.get("source_sha256_16"):
+    h = hashlib.sha256()
+    for f in ent["sources"]:
+        h.update(open(os.path.join(ROOT, "layer_pipeline_staged_gb300", "csrc", f), "rb").read())
+    if h.hexdigest()[:16] != ent.get("sources_sha256_16"):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -383,7 +385,7 @@ def main():
                      "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
                      else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_us": dom_avg_s * 1e6,
-                     "launches_timed": dom_n, "traffic": kernel_traffic(dom, wl)},
+                     "launches_timed": dom_n, "traffic": kernel_traffic(dom, cfg.name)},
         "cpu_baseline": cpu,
         "e2e": {"value": n * B * K / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": B * 8,
                 "d2h_bytes_per_step": B * V * 4,
