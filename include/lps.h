@@ -253,6 +253,32 @@ int model_attn_out(const lps_model* m, int layer, int b, float* host);
 int model_time_kernel(lps_model* m, int kind, int enable);
 int model_kernel_time(lps_model* m, int kind, double* total_ms, uint64_t* launches);
 
+/* ---- launch trace --------------------------------------------------------- */
+
+/* One launch of the decode step: its kernel family, where it ran, and the
+ * device clock (%globaltimer, ns) of its earliest CTA start and latest warp
+ * end, so that overlapping launches (stages, programmatic dependent launch)
+ * show as they ran. */
+typedef struct {
+  int32_t kind;      /* LPS_KERNEL_* */
+  int32_t stage;
+  int32_t layer;     /* -1 for the embedding and the LM head */
+  int32_t step;      /* the model's step counter when the launch was enqueued */
+  uint64_t start_ns;
+  uint64_t end_ns;   /* 0 if the launch has not finished or left early */
+} lps_trace_record;
+
+/* Record every launch of the following steps, up to `capacity` records (a
+ * device buffer of 16 bytes per record, from the model's allocator; launches
+ * past it are counted as dropped). Each kernel then does two extra atomics
+ * per CTA; results are unchanged. LPS_EINVAL for capacity < 1. */
+int model_trace_enable(lps_model* m, int capacity);
+/* Synchronize, copy up to max_records records (launch order) into out, return
+ * their count and the dropped count, and start a new recording. */
+int model_trace_read(lps_model* m, lps_trace_record* out, int max_records, int* n_records, uint64_t* dropped);
+/* Stop recording and release the buffer. */
+int model_trace_disable(lps_model* m);
+
 /* ---- allocation-free attention ------------------------------------------ */
 
 /* The paper has no counterpart to this entry point. It serves callers that may

@@ -227,6 +227,25 @@ class Model:
         _check(load().model_attn_out(self.h, layer, b, _ptr(out)))
         return out
 
+    def trace_enable(self, capacity: int = 1 << 16):
+        """Record every launch of the following steps (kind, stage, layer, step, device start/end ns)."""
+        _check(load().model_trace_enable(self.h, capacity))
+
+    def trace_read(self) -> tuple:
+        """(records, dropped): the recorded launches in launch order as a list of dicts; restarts the recording."""
+        cap = 1 << 20
+        buf = (_capi.TraceRecord * cap)()
+        n = ctypes.c_int()
+        dropped = ctypes.c_uint64()
+        _check(load().model_trace_read(self.h, buf, cap, ctypes.byref(n), ctypes.byref(dropped)))
+        names = {v: k for k, v in KERNELS.items()}
+        recs = [dict(kind=names.get(r.kind, r.kind), stage=r.stage, layer=r.layer, step=r.step, start_ns=r.start_ns,
+                     end_ns=r.end_ns) for r in buf[: n.value]]
+        return recs, dropped.value
+
+    def trace_disable(self):
+        _check(load().model_trace_disable(self.h))
+
     def set_serial_steps(self, serial: bool):
         _check(load().model_set_serial_steps(self.h, int(serial)))
 

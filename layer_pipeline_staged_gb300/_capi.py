@@ -31,7 +31,7 @@ EXPORTS = (
     "pending_wait", "pending_free", "decode_step_device", "model_synchronize", "model_stream",
     "last_error_string", "model_stats", "model_kv_export", "model_kv_import", "model_attn_out",
     "model_time_kernel", "model_kernel_time", "model_set_serial_steps", "attention_decode_noalloc", "attention_decode_noalloc_error",
-    "attention_decode_noalloc_scratch_bytes",
+    "attention_decode_noalloc_scratch_bytes", "model_trace_enable", "model_trace_read", "model_trace_disable",
 )
 
 
@@ -64,6 +64,11 @@ FREE_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_void_p)
 class Runtime(ctypes.Structure):
     _fields_ = [("device", ctypes.c_int), ("alloc", ALLOC_FN), ("free", FREE_FN), ("alloc_ctx", ctypes.c_void_p),
                 ("streams", ctypes.POINTER(ctypes.c_void_p))]
+
+
+class TraceRecord(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("stage", ctypes.c_int32), ("layer", ctypes.c_int32),
+                ("step", ctypes.c_int32), ("start_ns", ctypes.c_uint64), ("end_ns", ctypes.c_uint64)]
 
 
 class Stats(ctypes.Structure):
@@ -108,6 +113,9 @@ def load(path: str = LIB_PATH):
         "model_time_kernel": (i, [vp, i, i]),
         "model_set_serial_steps": (i, [vp, i]),
         "model_kernel_time": (i, [vp, i, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_uint64)]),
+        "model_trace_enable": (i, [vp, i]),
+        "model_trace_read": (i, [vp, ctypes.POINTER(TraceRecord), i, ctypes.POINTER(i), ctypes.POINTER(ctypes.c_uint64)]),
+        "model_trace_disable": (i, [vp]),
         "attention_decode_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, i, vp, vp]),
         "attention_decode_noalloc_error": (ctypes.c_char_p, []),
         "attention_decode_noalloc_scratch_bytes": (ctypes.c_longlong, [i, i, i, i, i]),

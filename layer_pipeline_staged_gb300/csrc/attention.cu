@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const __grid_constant
   AttnSmem<HD, G>& sm = *reinterpret_cast<AttnSmem<HD, G>*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g8 = lane >> 2, t4 = lane & 3;  // mma fragment coordinates
+  trace_start(p.trace);
   const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int pos = p.pos[b];
   const int n_total = pos + 1;
@@ -445,6 +446,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const __grid_constant
     if (tid == 0) p.counter[b * p.nkv + g] = 0;
   }
   pdl_launch_dependents();
+  trace_end(p.trace);
 }
 
 template <int HD, int G>

@@ -8,6 +8,7 @@ namespace {
 
 template <bool INT8>
 __global__ void __launch_bounds__(256) embed_kernel(const __grid_constant__ EmbedParams p) {
+  trace_start(p.trace);
   pdl_launch_dependents();
   const int b = blockIdx.y;
   const int tok = p.tok_dev ? p.tok_dev[b] : p.tok[b];
@@ -31,6 +32,7 @@ __global__ void __launch_bounds__(256) embed_kernel(const __grid_constant__ Embe
     }
     *reinterpret_cast<float4*>(h + i) = v;
   }
+  trace_end(p.trace);
 }
 
 }  // namespace

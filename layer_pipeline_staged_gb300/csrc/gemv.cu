@@ -91,6 +91,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) gemv_kernel(const __g
   uint64_t* empty = full + p.nbuf;
   float* nred = reinterpret_cast<float*>(empty + p.nbuf);
 
+  trace_start(p.trace);
   if (tid == 0) {
     for (int i = 0; i < p.nbuf; ++i) {
       mbar_init(&full[i], 1);
@@ -246,6 +247,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) gemv_kernel(const __g
       }
     }
   }
+  trace_end(p.trace);
 }
 
 int g_max_smem = 0;

@@ -44,6 +44,7 @@ struct GemvParams {
   int nq, nkv, hd, max_ctx, pos;
   int nwarps;           // consumer warps (set from the plan at launch)
   int* status;
+  unsigned long long* trace;  // launch trace record, or nullptr
 };
 
 struct GemvPlan {
@@ -76,6 +77,7 @@ struct SkinnyParams {
   int nq, nkv, hd, max_ctx;
   int pos[kMaxBatch];
   int* status;
+  unsigned long long* trace;  // launch trace record, or nullptr
 };
 struct SkinnyPlan {
   int grid, smem, kc, units;
@@ -113,6 +115,7 @@ struct AttnParams {
   int pos[kMaxBatch];
   float scale;                 // 1/sqrt(hd)
   int* status;
+  unsigned long long* trace;  // launch trace record, or nullptr
 };
 int attn_sub_tile(int hd);
 int attn_chunk(int hd, int nkv, int batch, int max_pos, int num_sms);
@@ -128,6 +131,7 @@ struct EmbedParams {
   int d, vocab, batch;
   float* h;              // [B][d]
   int* status;
+  unsigned long long* trace;  // launch trace record, or nullptr
 };
 cudaError_t launch_embed(const EmbedParams& p, bool int8, cudaStream_t s, bool pdl);
 

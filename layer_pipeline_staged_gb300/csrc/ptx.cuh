@@ -68,6 +68,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
   return true;
 }
 
+// Launch tracing: a record is two 64-bit words, both zero before the launch:
+// word 0 collects ~(earliest start) by atomicMax, word 1 the latest end, in
+// %globaltimer nanoseconds. t == nullptr when tracing is off.
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void trace_start(unsigned long long* t) {
+  if (t && threadIdx.x == 0) atomicMax(t, ~global_ns());
+}
+__device__ __forceinline__ void trace_end(unsigned long long* t) {
+  if (t && (threadIdx.x & 31) == 0) atomicMax(t + 1, global_ns());
+}
+
 // L2 policy that lets streamed-once data (weights, KV rows) be evicted first.
 __device__ __forceinline__ uint64_t l2_evict_first() {
   uint64_t pol;

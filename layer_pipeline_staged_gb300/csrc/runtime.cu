@@ -225,6 +225,11 @@ struct lps_model {
   bool failed = false;
   int attn_max_chunks = 0;
   KTimer timers[7];
+  // launch trace: device records [cap][2] (zeroed), host metadata per record
+  unsigned long long* trace_dev = nullptr;
+  int trace_cap = 0, trace_n = 0;
+  uint64_t trace_dropped = 0;
+  std::vector<lps_trace_record> trace_meta;
 
   cudaStream_t stream(int s) const { return single ? st[0].stream : st[s].stream; }
 };
@@ -437,6 +442,22 @@ bool make_kv_map(CUtensorMap* map, void* base, int hd, unsigned long long rows, 
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The trace record of the next launch (two zeroed 64-bit words), or nullptr.
+unsigned long long* trace_slot(lps_model* m, int kind, int stage, int layer) {
+  if (!m->trace_dev) return nullptr;
+  if (m->trace_n >= m->trace_cap) {
+    ++m->trace_dropped;
+    return nullptr;
+  }
+  lps_trace_record r{};
+  r.kind = kind;
+  r.stage = stage;
+  r.layer = layer;
+  r.step = static_cast<int32_t>(m->step_count);
+  m->trace_meta.push_back(r);
+  return m->trace_dev + 2 * static_cast<size_t>(m->trace_n++);
 }
 
 int timer_begin(lps_model* m, int kind, cudaStream_t s, cudaEvent_t* stop) {
@@ -843,9 +864,11 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
   bool pdl = false;
   uint64_t launches = 0;
   cudaEvent_t stop;
+  int s_trace = 0, layer_trace = -1;  // stage and layer of the next launch, for the trace
 
-#define LAUNCH(kind, stream, call)                                          \
+#define LAUNCH(kind, stream, params, call)                                  \
   do {                                                                      \
+    (params).trace = trace_slot(m, kind, s_trace, layer_trace);             \
     if (timer_begin(m, kind, stream, &stop)) return fail(LPS_ECUDA, FN, "timer event"); \
     cudaError_t e_ = (call);                                                \
     if (e_ != cudaSuccess) {                                                \
@@ -861,6 +884,8 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
     StageDev& S = m->st[s];
     const cudaStream_t cs = m->stream(s);
     pdl = false;
+    s_trace = s;
+    layer_trace = -1;
     if (!m->single) {
       if (s > 0) CK(cudaStreamWaitEvent(cs, m->bd[s - 1].ev_tx[par], 0), "wait ev_tx");
       if (s + 1 < N) CK(cudaStreamWaitEvent(cs, m->bd[s].ev_rx[par], 0), "wait ev_rx");
@@ -881,11 +906,12 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
       ep.batch = B;
       ep.h = S.h;
       ep.status = m->status_dev;
-      LAUNCH(LPS_KERNEL_EMBED, cs, launch_embed(ep, m->int8, cs, pdl));
+      LAUNCH(LPS_KERNEL_EMBED, cs, ep, launch_embed(ep, m->int8, cs, pdl));
     }
     for (int l = S.l0; l < S.l1; ++l) {
       const LayerDev& L = S.layers[l - S.l0];
       const bool first = (l == S.l0), last = (l == S.l1 - 1);
+      layer_trace = l;
       const float* hin = first ? h_first : S.h;
       float* o_buf = L.o_keep ? L.o_keep : S.o;
       // RMSNorm -> QKV -> RoPE -> q and KV-cache row pos (per sequence)
@@ -898,7 +924,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
         p.kc = L.kc;
         p.vc = L.vc;
         p.rope = S.rope;
-        LAUNCH(LPS_KERNEL_QKV, cs, launch_skinny(p, kEpiQkv, true, m->int8, S.sk_qkv, cs, pdl));
+        LAUNCH(LPS_KERNEL_QKV, cs, p, launch_skinny(p, kEpiQkv, true, m->int8, S.sk_qkv, cs, pdl));
       }
       for (int b = 0; b < (m->skinny ? 0 : B); ++b) {
         GemvParams p{};
@@ -923,7 +949,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
         p.max_ctx = d.max_ctx;
         p.pos = pos[b];
         p.status = m->status_dev;
-        LAUNCH(LPS_KERNEL_QKV, cs, launch_gemv(p, kEpiQkv, true, m->int8, S.plan_qkv, cs, pdl));
+        LAUNCH(LPS_KERNEL_QKV, cs, p, launch_gemv(p, kEpiQkv, true, m->int8, S.plan_qkv, cs, pdl));
       }
       // split-K attention over [0, pos]
       {
@@ -945,7 +971,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
         for (int b = 0; b < B; ++b) ap.pos[b] = pos[b];
         ap.scale = 1.0f / std::sqrt(static_cast<float>(hd));
         ap.status = m->status_dev;
-        LAUNCH(LPS_KERNEL_ATTN, cs, launch_attention(ap, B, max_pos, cs, pdl));
+        LAUNCH(LPS_KERNEL_ATTN, cs, ap, launch_attention(ap, B, max_pos, cs, pdl));
       }
       // o-proj + residual (the first layer of a later stage reads the boundary slot)
       if (m->skinny) {
@@ -954,7 +980,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
         p.h_in = hin;
         p.h_out = S.h;
         p.out_stride = E;
-        LAUNCH(LPS_KERNEL_OPROJ, cs, launch_skinny(p, kEpiResidual, false, m->int8, S.sk_o, cs, pdl));
+        LAUNCH(LPS_KERNEL_OPROJ, cs, p, launch_skinny(p, kEpiResidual, false, m->int8, S.sk_o, cs, pdl));
       }
       for (int b = 0; b < (m->skinny ? 0 : B); ++b) {
         GemvParams p{};
@@ -970,7 +996,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
         p.h_in = hin + static_cast<size_t>(b) * E;
         p.h_out = S.h + static_cast<size_t>(b) * E;
         p.status = m->status_dev;
-        LAUNCH(LPS_KERNEL_OPROJ, cs, launch_gemv(p, kEpiResidual, false, m->int8, S.plan_o, cs, pdl));
+        LAUNCH(LPS_KERNEL_OPROJ, cs, p, launch_gemv(p, kEpiResidual, false, m->int8, S.plan_o, cs, pdl));
       }
       if (first && s > 0 && !m->single) CK(cudaEventRecord(m->bd[s - 1].ev_rx[par], cs), "record ev_rx");
       // RMSNorm -> gate/up -> SwiGLU
@@ -980,7 +1006,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
         p.gain = L.ffn_norm;
         p.out = S.a;
         p.out_stride = d.ffn;
-        LAUNCH(LPS_KERNEL_GATEUP, cs, launch_skinny(p, kEpiSwiglu, true, m->int8, S.sk_gu, cs, pdl));
+        LAUNCH(LPS_KERNEL_GATEUP, cs, p, launch_skinny(p, kEpiSwiglu, true, m->int8, S.sk_gu, cs, pdl));
       }
       for (int b = 0; b < (m->skinny ? 0 : B); ++b) {
         GemvParams p{};
@@ -997,7 +1023,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
         p.eps = d.rms_eps;
         p.out = S.a + static_cast<size_t>(b) * d.ffn;
         p.status = m->status_dev;
-        LAUNCH(LPS_KERNEL_GATEUP, cs, launch_gemv(p, kEpiSwiglu, true, m->int8, S.plan_gu, cs, pdl));
+        LAUNCH(LPS_KERNEL_GATEUP, cs, p, launch_gemv(p, kEpiSwiglu, true, m->int8, S.plan_gu, cs, pdl));
       }
       // down + residual (the last layer of an earlier stage writes the boundary slot)
       float* h_out = (last && s + 1 < N && !m->single) ? m->bd[s].slot[par] : S.h;
@@ -1007,7 +1033,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
         p.h_in = S.h;
         p.h_out = h_out;
         p.out_stride = E;
-        LAUNCH(LPS_KERNEL_DOWN, cs, launch_skinny(p, kEpiResidual, false, m->int8, S.sk_d, cs, pdl));
+        LAUNCH(LPS_KERNEL_DOWN, cs, p, launch_skinny(p, kEpiResidual, false, m->int8, S.sk_d, cs, pdl));
       }
       for (int b = 0; b < (m->skinny ? 0 : B); ++b) {
         GemvParams p{};
@@ -1023,7 +1049,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
         p.h_in = S.h + static_cast<size_t>(b) * E;
         p.h_out = h_out + static_cast<size_t>(b) * E;
         p.status = m->status_dev;
-        LAUNCH(LPS_KERNEL_DOWN, cs, launch_gemv(p, kEpiResidual, false, m->int8, S.plan_d, cs, pdl));
+        LAUNCH(LPS_KERNEL_DOWN, cs, p, launch_gemv(p, kEpiResidual, false, m->int8, S.plan_d, cs, pdl));
       }
     }
     if (s + 1 < N) {
@@ -1041,13 +1067,15 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
   {
     StageDev& S = m->st[N - 1];
     const cudaStream_t cs = m->stream(N - 1);
+    s_trace = N - 1;
+    layer_trace = -1;
     if (m->skinny) {
       SkinnyParams p = skinny_params(m, S.head, S.head_s, d.vocab, E, pos);
       p.x = S.h;
       p.gain = S.out_norm;
       p.out = logits_dev;
       p.out_stride = d.vocab;
-      LAUNCH(LPS_KERNEL_HEAD, cs, launch_skinny(p, kEpiStore, true, m->int8, S.sk_head, cs, pdl));
+      LAUNCH(LPS_KERNEL_HEAD, cs, p, launch_skinny(p, kEpiStore, true, m->int8, S.sk_head, cs, pdl));
     }
     for (int b = 0; b < (m->skinny ? 0 : B); ++b) {
       GemvParams p{};
@@ -1064,7 +1092,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
       p.eps = d.rms_eps;
       p.out = logits_dev + static_cast<size_t>(b) * d.vocab;
       p.status = m->status_dev;
-      LAUNCH(LPS_KERNEL_HEAD, cs, launch_gemv(p, kEpiStore, true, m->int8, S.plan_head, cs, pdl));
+      LAUNCH(LPS_KERNEL_HEAD, cs, p, launch_gemv(p, kEpiStore, true, m->int8, S.plan_head, cs, pdl));
     }
     if (N > 1 && !m->single && !m->overlap) CK(cudaEventRecord(m->ev_step, cs), "record step event");
   }
@@ -1295,6 +1323,60 @@ extern "C" int model_set_serial_steps(lps_model* m, int serial) {
   const int rc = model_synchronize(m);
   if (rc) return rc;
   m->overlap = serial == 0;
+  return LPS_OK;
+}
+
+extern "C" int model_trace_enable(lps_model* m, int capacity) {
+  static const char* FN = "model_trace_enable";
+  if (!m || capacity < 1) return fail(LPS_EINVAL, FN, "model and capacity >= 1 are required");
+  int rc = model_trace_disable(m);
+  if (rc) return rc;
+  const size_t bytes = 16 * static_cast<size_t>(capacity);
+  m->trace_dev = static_cast<unsigned long long*>(dev_alloc(m, bytes));
+  if (!m->trace_dev) return fail(LPS_ENOMEM, FN, "trace buffer allocation failed");
+  CK(cudaMemset(m->trace_dev, 0, bytes), "cudaMemset");
+  m->trace_cap = capacity;
+  m->trace_n = 0;
+  m->trace_dropped = 0;
+  m->trace_meta.clear();
+  return LPS_OK;
+}
+
+extern "C" int model_trace_read(lps_model* m, lps_trace_record* out, int max_records, int* n_records,
+                                uint64_t* dropped) {
+  static const char* FN = "model_trace_read";
+  if (!m || !n_records || (max_records > 0 && !out)) return fail(LPS_EINVAL, FN, "bad argument");
+  if (!m->trace_dev) return fail(LPS_EINVAL, FN, "tracing is not enabled");
+  int rc = model_synchronize(m);
+  if (rc) return rc;
+  const int n = m->trace_n < max_records ? m->trace_n : (max_records > 0 ? max_records : 0);
+  std::vector<unsigned long long> words(2 * static_cast<size_t>(m->trace_n));
+  if (m->trace_n)
+    CK(cudaMemcpy(words.data(), m->trace_dev, 16 * static_cast<size_t>(m->trace_n), cudaMemcpyDeviceToHost),
+       "cudaMemcpy");
+  for (int i = 0; i < n; ++i) {
+    out[i] = m->trace_meta[i];
+    out[i].start_ns = words[2 * i] ? ~words[2 * i] : 0;
+    out[i].end_ns = words[2 * i + 1];
+  }
+  *n_records = n;
+  if (dropped) *dropped = m->trace_dropped;
+  CK(cudaMemset(m->trace_dev, 0, 16 * static_cast<size_t>(m->trace_cap)), "cudaMemset");
+  m->trace_n = 0;
+  m->trace_dropped = 0;
+  m->trace_meta.clear();
+  return LPS_OK;
+}
+
+extern "C" int model_trace_disable(lps_model* m) {
+  if (!m) return fail(LPS_EINVAL, "model_trace_disable", "model is NULL");
+  if (!m->trace_dev) return LPS_OK;
+  int rc = model_synchronize(m);
+  if (rc) return rc;
+  dev_free(m, m->trace_dev);
+  m->trace_dev = nullptr;
+  m->trace_cap = m->trace_n = 0;
+  m->trace_meta.clear();
   return LPS_OK;
 }
 

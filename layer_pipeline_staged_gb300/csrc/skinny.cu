@@ -172,6 +172,7 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, 1) skinny_kernel(const __gr
   // warp w's k-chunks in a pass: w + 8 n for n < ng(w)
   auto warp_chunks = [&](int w) { return w < nk ? (nk - 1 - w) / NW + 1 : 0; };
 
+  trace_start(p.trace);
   if (tid == 0) {
     for (int i = 0; i < NW * RC; ++i) {
       mbar_init(&full_all[i], 1);
@@ -480,6 +481,7 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, 1) skinny_kernel(const __gr
     if (pass + 1 < npass) named_bar_sync(kBarAll, nthreads);  // the scratch is written again next pass
   }
   if (bad) cp_async_wait_all();  // this thread's activation copies land before it leaves
+  trace_end(p.trace);
 }
 
 int g_max_smem = 0;
