@@ -142,6 +142,10 @@ __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const __grid_constant
     fence_mbar_init();
   }
   __syncthreads();
+  // Early, the next kernel's CTAs take SMs as soon as the CTAs here leave them
+  // (while the last CTAs combine); its own dependency wait still covers
+  // everything this kernel writes.
+  if (p.early_dependents) pdl_launch_dependents();
 
   auto issue = [&](int j) {
     const int slot = j % kRing;
@@ -445,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const __grid_constant
     }
     if (tid == 0) p.counter[b * p.nkv + g] = 0;
   }
-  pdl_launch_dependents();
+  if (!p.early_dependents) pdl_launch_dependents();
   trace_end(p.trace);
 }
 

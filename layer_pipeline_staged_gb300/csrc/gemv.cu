@@ -8,9 +8,14 @@
 //     contiguous byte range of the packed weights;
 //   - a producer warp streams that range through a ring of shared-memory
 //     buffers with 1D bulk copies (cp.async.bulk + mbarrier complete_tx) and
-//     an L2 evict-first hint; it fills the ring before the programmatic-
-//     dependent-launch wait, because weights never depend on the previous
-//     kernel, so the prefetch overlaps the previous kernel's tail;
+//     an L2 evict-first hint, lane L issuing the copies of slot L (one thread
+//     issues only about four copies per microsecond); it fills the ring
+//     without the programmatic-dependent-launch wait, because weights never
+//     depend on the previous kernel, so the prefetch overlaps that kernel's
+//     tail and this kernel's own prologue;
+//   - the consumers fetch the input vector (and the RMSNorm gain, before the
+//     dependency wait) in one round of loads per thread, and each lane loads
+//     its next unit's epilogue inputs before waiting for the buffer;
 //   - buffer i belongs to consumer warp i mod NW and sits in slot i mod nbuf,
 //     with nbuf a multiple of NW: every slot is owned by one warp, which waits
 //     on its phases strictly in order (a warp sharing slots with others could
@@ -71,7 +76,6 @@ __device__ __forceinline__ void consumers_sync(int nthreads) { named_bar_sync(1,
 template <bool INT8, bool NORM, int EPI, int RB>
 __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) gemv_kernel(const __grid_constant__ GemvParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  constexpr int EPC = Elem<INT8>::kPerChunk;
   constexpr int EB = Elem<INT8>::kBytes;
   constexpr int NP = Elem<INT8>::kPlanes;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -103,61 +107,142 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) gemv_kernel(const __g
   pdl_launch_dependents();
 
   if (warp == NW) {
-    // Producer: stream this CTA's weight range through the ring.
-    if (lane == 0) {
-      const uint64_t pol = l2_evict_first();
-      const uint8_t* src = static_cast<const uint8_t*>(p.w) + static_cast<size_t>(u0) * unit_bytes;
-      for (int i = 0; i < nbufs; ++i) {
-        const int slot = i % p.nbuf;
-        if (i >= p.nbuf && !mbar_wait(&empty[slot], ((i / p.nbuf) - 1) & 1)) {
-          report_error(p.status, kErrWaitEmpty | ((EPI + 1) << 8));
-          break;
-        }
+    // Producer: lane L streams the buffers of slot L (L, L + nbuf, ...) of this
+    // CTA's weight range. The lanes poll their slots together, so the first
+    // fill goes out in one instruction and no lane's wait blocks another's copy.
+    const uint64_t pol = l2_evict_first();
+    const uint8_t* src = static_cast<const uint8_t*>(p.w) + static_cast<size_t>(u0) * unit_bytes;
+    int i = lane;
+    bool done = lane >= p.nbuf || i >= nbufs;
+    long long t0 = cycles();
+    while (true) {
+      bool ready = false;
+      if (!done) ready = i < p.nbuf || mbar_test(&empty[lane], ((i / p.nbuf) - 1) & 1);
+      if (ready) {
         const int nu = min(ups, nunits - i * ups);
         const uint32_t bytes = static_cast<uint32_t>(nu) * unit_bytes;
-        mbar_arrive_expect_tx(&full[slot], bytes);
-        bulk_g2s(smem + static_cast<size_t>(slot) * buf_bytes, src + static_cast<size_t>(i) * buf_bytes, bytes,
-                 &full[slot], pol);
+        mbar_arrive_expect_tx(&full[lane], bytes);
+        bulk_g2s(smem + static_cast<size_t>(lane) * buf_bytes, src + static_cast<size_t>(i) * buf_bytes, bytes,
+                 &full[lane], pol);
+        i += p.nbuf;
+        done = i >= nbufs;
+        t0 = cycles();
+      } else if (!done && cycles() - t0 > kWaitLimitCycles) {
+        report_error(p.status, kErrWaitEmpty | ((EPI + 1) << 8));
+        done = true;
       }
+      if (__all_sync(0xffffffffu, done)) break;
+      if (!__any_sync(0xffffffffu, ready)) __nanosleep(64);  // nothing to issue yet
     }
     return;
   }
 
-  // Consumers: the input vector into shared memory (after the previous kernel is visible).
-  pdl_wait();
+  // Consumers: the input vector into shared memory. The RMSNorm gain does not
+  // depend on the previous kernel, so it is fetched before the dependency wait;
+  // the vector itself is fetched after it, every load of a thread issued at once.
   const int nthreads = NW * 32;
   const int K4 = p.K / 4;
   const float4* src4 = reinterpret_cast<const float4*>(NORM ? p.h : p.x);
-  float inv = 1.f;
-  if (NORM) {
-    float ss = 0.f;
-    for (int k4 = tid; k4 < K4; k4 += nthreads) {
-      const float4 v = src4[k4];
-      ss = fmaf(v.x, v.x, ss);
-      ss = fmaf(v.y, v.y, ss);
-      ss = fmaf(v.z, v.z, ss);
-      ss = fmaf(v.w, v.w, ss);
-    }
-    ss = warp_sum(ss);
-    if (lane == 0) nred[warp] = ss;
-    consumers_sync(nthreads);
-    float tot = 0.f;
-    for (int w = 0; w < NW; ++w) tot += nred[w];
-    inv = 1.0f / sqrtf(tot / static_cast<float>(p.K) + p.eps);
-  }
   const float4* g4 = reinterpret_cast<const float4*>(p.gain);
-  for (int k4 = tid; k4 < K4; k4 += nthreads) {
-    float4 v = src4[k4];
-    if (NORM) {
-      const float4 g = g4[k4];
-      v = make_float4(v.x * inv * g.x, v.y * inv * g.y, v.z * inv * g.z, v.w * inv * g.w);
+  constexpr int XR = NORM ? 8 : 20;  // float4 per thread held in registers
+  const bool in_regs = K4 <= XR * nthreads;
+  float4 gr[NORM ? XR : 1];
+  if (NORM && in_regs) {
+#pragma unroll
+    for (int r = 0; r < XR; ++r) {
+      const int k4 = tid + r * nthreads;
+      if (k4 < K4) gr[r] = g4[k4];
     }
-    xs[(k4 % NP) * nch + k4 / NP] = v;  // plane (k4 mod NP) of chunk k4 / NP
+  }
+  pdl_wait();
+  if (in_regs) {
+    float4 xr[XR];
+#pragma unroll
+    for (int r = 0; r < XR; ++r) {
+      const int k4 = tid + r * nthreads;
+      if (k4 < K4) xr[r] = src4[k4];
+    }
+    if (NORM) {
+      float ss = 0.f;
+#pragma unroll
+      for (int r = 0; r < XR; ++r) {
+        if (tid + r * nthreads < K4) {
+          ss = fmaf(xr[r].x, xr[r].x, ss);
+          ss = fmaf(xr[r].y, xr[r].y, ss);
+          ss = fmaf(xr[r].z, xr[r].z, ss);
+          ss = fmaf(xr[r].w, xr[r].w, ss);
+        }
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) nred[warp] = ss;
+      consumers_sync(nthreads);
+      float tot = 0.f;
+      for (int w = 0; w < NW; ++w) tot += nred[w];
+      const float inv = 1.0f / sqrtf(tot / static_cast<float>(p.K) + p.eps);
+#pragma unroll
+      for (int r = 0; r < XR; ++r) {
+        const float4 g = gr[NORM ? r : 0];
+        xr[r] = make_float4(xr[r].x * inv * g.x, xr[r].y * inv * g.y, xr[r].z * inv * g.z, xr[r].w * inv * g.w);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < XR; ++r) {
+      const int k4 = tid + r * nthreads;
+      if (k4 < K4) xs[(k4 % NP) * nch + k4 / NP] = xr[r];
+    }
+  } else {
+    // vectors too long for registers: passes over global memory
+    float inv = 1.f;
+    if (NORM) {
+      float ss = 0.f;
+      for (int k4 = tid; k4 < K4; k4 += nthreads) {
+        const float4 v = src4[k4];
+        ss = fmaf(v.x, v.x, ss);
+        ss = fmaf(v.y, v.y, ss);
+        ss = fmaf(v.z, v.z, ss);
+        ss = fmaf(v.w, v.w, ss);
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) nred[warp] = ss;
+      consumers_sync(nthreads);
+      float tot = 0.f;
+      for (int w = 0; w < NW; ++w) tot += nred[w];
+      inv = 1.0f / sqrtf(tot / static_cast<float>(p.K) + p.eps);
+    }
+    for (int k4 = tid; k4 < K4; k4 += nthreads) {
+      float4 v = src4[k4];
+      if (NORM) {
+        const float4 g = g4[k4];
+        v = make_float4(v.x * inv * g.x, v.y * inv * g.y, v.z * inv * g.z, v.w * inv * g.w);
+      }
+      xs[(k4 % NP) * nch + k4 / NP] = v;
+    }
   }
   consumers_sync(nthreads);
 
   for (int i = warp; i < nbufs; i += NW) {
     const int slot = i % p.nbuf;
+    const int nu = min(ups, nunits - i * ups);
+    // Lane j's epilogue inputs for unit j of this buffer, loaded before the
+    // wait so that their latency hides behind it and the dot products.
+    float s0 = 1.f, s1 = 1.f, e0 = 0.f, e1 = 0.f;
+    if (lane < nu) {
+      const int u = u0 + i * ups + lane;
+      if (INT8) {
+        s0 = p.wscale[u * p.unit_rows];
+        if (EPI == kEpiQkv || EPI == kEpiSwiglu) s1 = p.wscale[u * p.unit_rows + 1];
+      }
+      if (EPI == kEpiQkv) {
+        const int half = p.hd >> 1;
+        const int hh = u / half;
+        if (hh < p.nq + p.nkv) {
+          const float2 cs = p.rope[u - hh * half];
+          e0 = cs.x;
+          e1 = cs.y;
+        }
+      }
+      if (EPI == kEpiResidual) e0 = p.h_in[u];
+    }
     if (!mbar_wait(&full[slot], (i / p.nbuf) & 1)) {
       // A copy never arrived: record it, let this warp drain its own later buffers, stop.
       if (lane == 0) {
@@ -171,7 +256,6 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) gemv_kernel(const __g
       }
       return;
     }
-    const int nu = min(ups, nunits - i * ups);
     const int rows = nu * p.unit_rows;
     const uint8_t* buf = smem + static_cast<size_t>(slot) * buf_bytes;
     float acc[RB];
@@ -217,28 +301,26 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) gemv_kernel(const __g
           y0 = acc[j];
         }
         if (INT8) {
-          y0 *= p.wscale[u * p.unit_rows];
-          if (EPI == kEpiQkv || EPI == kEpiSwiglu) y1 *= p.wscale[u * p.unit_rows + 1];
+          y0 *= s0;
+          if (EPI == kEpiQkv || EPI == kEpiSwiglu) y1 *= s1;
         }
         if (EPI == kEpiQkv) {
           const int half = p.hd >> 1;
           const int hh = u / half, ii = u - hh * half;
           if (hh < p.nq) {
-            const float2 cs = p.rope[ii];
-            p.out[hh * p.hd + ii] = y0 * cs.x - y1 * cs.y;
-            p.out[hh * p.hd + ii + half] = y0 * cs.y + y1 * cs.x;
+            p.out[hh * p.hd + ii] = y0 * e0 - y1 * e1;
+            p.out[hh * p.hd + ii + half] = y0 * e1 + y1 * e0;
           } else if (hh < p.nq + p.nkv) {
-            const float2 cs = p.rope[ii];
             const size_t base = (static_cast<size_t>(hh - p.nq) * p.max_ctx + p.pos) * p.hd;
-            p.kc[base + ii] = __float2bfloat16_rn(y0 * cs.x - y1 * cs.y);
-            p.kc[base + ii + half] = __float2bfloat16_rn(y0 * cs.y + y1 * cs.x);
+            p.kc[base + ii] = __float2bfloat16_rn(y0 * e0 - y1 * e1);
+            p.kc[base + ii + half] = __float2bfloat16_rn(y0 * e1 + y1 * e0);
           } else {
             const size_t base = (static_cast<size_t>(hh - p.nq - p.nkv) * p.max_ctx + p.pos) * p.hd;
             p.vc[base + ii] = __float2bfloat16_rn(y0);
             p.vc[base + ii + half] = __float2bfloat16_rn(y1);
           }
         } else if (EPI == kEpiResidual) {
-          p.h_out[u] = p.h_in[u] + y0;
+          p.h_out[u] = e0 + y0;
         } else if (EPI == kEpiSwiglu) {
           p.out[u] = y0 / (1.0f + expf(-y0)) * y1;
         } else {

@@ -114,6 +114,8 @@ struct AttnParams {
   int chunk;                   // positions per CTA (multiple of the sub-tile)
   int pos[kMaxBatch];
   float scale;                 // 1/sqrt(hd)
+  int early_dependents;        // 1: let the next kernel launch once every CTA has started
+                               // (pays when it is the batch-1 GEMV), 0: once every CTA ends
   int* status;
   unsigned long long* trace;  // launch trace record, or nullptr
 };

@@ -71,6 +71,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
 // Launch tracing: a record is two 64-bit words, both zero before the launch:
 // word 0 collects ~(earliest start) by atomicMax, word 1 the latest end, in
 // %globaltimer nanoseconds. t == nullptr when tracing is off.
+// One non-blocking look at phase `parity` of `bar`: true once it has completed.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -107,6 +120,14 @@ __device__ __forceinline__ void bulk_g2s_plain(void* dst, const void* src, uint3
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
+
+// 16-byte global -> shared copy through L2 (bytes < 16 zero-fill the rest)
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_but_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // Programmatic dependent launch: let the next kernel in the stream start its
 // prologue, and wait until the previous kernel's results are visible.

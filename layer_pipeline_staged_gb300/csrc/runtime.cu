@@ -970,6 +970,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
         ap.chunk = chunk;
         for (int b = 0; b < B; ++b) ap.pos[b] = pos[b];
         ap.scale = 1.0f / std::sqrt(static_cast<float>(hd));
+        ap.early_dependents = m->skinny ? 0 : 1;  // the GEMV o-proj follows
         ap.status = m->status_dev;
         LAUNCH(LPS_KERNEL_ATTN, cs, ap, launch_attention(ap, B, max_pos, cs, pdl));
       }

@@ -83,18 +83,6 @@ __device__ __forceinline__ bool bar_or(int id, int nthreads, bool bad) {
 }
 
 // Non-blocking test of phase `parity` of `bar`.
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Wait for phase `parity` of `bar`, the thread suspended in hardware between
 // checks (up to 20 us each); false after `limit` cycles.
 __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, long long limit = kWaitLimitCycles) {
@@ -115,12 +103,6 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, 
 
 // 16-byte asynchronous copy global -> shared by this thread; `bytes` (0 or 16)
 // are read, the rest of the 16 is zero-filled.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_but_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // Shared-memory map of one CTA, in bytes; the same on host and device.
 struct Layout {
