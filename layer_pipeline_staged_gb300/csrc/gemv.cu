@@ -8,11 +8,10 @@
 //     contiguous byte range of the packed weights;
 //   - a producer warp streams that range through a ring of shared-memory
 //     buffers with 1D bulk copies (cp.async.bulk + mbarrier complete_tx) and
-//     an L2 evict-first hint, lane L issuing the copies of slot L (one thread
-//     issues only about four copies per microsecond); it fills the ring
-//     without the programmatic-dependent-launch wait, because weights never
-//     depend on the previous kernel, so the prefetch overlaps that kernel's
-//     tail and this kernel's own prologue;
+//     an L2 evict-first hint; it fills the ring without the programmatic-
+//     dependent-launch wait, because weights never depend on the previous
+//     kernel, so the prefetch overlaps that kernel's tail and this kernel's
+//     own prologue;
 //   - the consumers fetch the input vector (and the RMSNorm gain, before the
 //     dependency wait) in one round of loads per thread, and each lane loads
 //     its next unit's epilogue inputs before waiting for the buffer;
@@ -36,6 +35,10 @@ namespace lps {
 namespace {
 
 constexpr int kMaxWarps = 8;        // consumer warps
+// Producer lanes issuing copies. More lanes fill the ring faster at kernel
+// start but measured slower on whole decode steps: the burst queues ahead of
+// the previous kernel's completion and of this kernel's input-vector loads.
+constexpr int kIssueLanes = 1;
 constexpr int kMaxBuf = 16;
 constexpr int kMaxRows = 4;         // rows per buffer
 constexpr int kBufTarget = 16 * 1024;
@@ -107,24 +110,27 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) gemv_kernel(const __g
   pdl_launch_dependents();
 
   if (warp == NW) {
-    // Producer: lane L streams the buffers of slot L (L, L + nbuf, ...) of this
-    // CTA's weight range. The lanes poll their slots together, so the first
-    // fill goes out in one instruction and no lane's wait blocks another's copy.
+    // Producer: lane l of the first IL lanes streams buffers l, l + IL, ...
+    // of this CTA's weight range (buffer i into slot i mod nbuf, every slot
+    // owned by one lane). The lanes poll their slots together, so no lane's
+    // wait blocks another's copy.
+    const int IL = p.nbuf % kIssueLanes == 0 ? kIssueLanes : 1;
     const uint64_t pol = l2_evict_first();
     const uint8_t* src = static_cast<const uint8_t*>(p.w) + static_cast<size_t>(u0) * unit_bytes;
     int i = lane;
-    bool done = lane >= p.nbuf || i >= nbufs;
+    bool done = lane >= IL || i >= nbufs;
     long long t0 = cycles();
     while (true) {
       bool ready = false;
-      if (!done) ready = i < p.nbuf || mbar_test(&empty[lane], ((i / p.nbuf) - 1) & 1);
+      const int slot = i % p.nbuf;
+      if (!done) ready = i < p.nbuf || mbar_test(&empty[slot], ((i / p.nbuf) - 1) & 1);
       if (ready) {
         const int nu = min(ups, nunits - i * ups);
         const uint32_t bytes = static_cast<uint32_t>(nu) * unit_bytes;
-        mbar_arrive_expect_tx(&full[lane], bytes);
-        bulk_g2s(smem + static_cast<size_t>(lane) * buf_bytes, src + static_cast<size_t>(i) * buf_bytes, bytes,
-                 &full[lane], pol);
-        i += p.nbuf;
+        mbar_arrive_expect_tx(&full[slot], bytes);
+        bulk_g2s(smem + static_cast<size_t>(slot) * buf_bytes, src + static_cast<size_t>(i) * buf_bytes, bytes,
+                 &full[slot], pol);
+        i += IL;
         done = i >= nbufs;
         t0 = cycles();
       } else if (!done && cycles() - t0 > kWaitLimitCycles) {
@@ -382,12 +388,12 @@ GemvPlan gemv_plan(int rows, int K, int unit_rows, bool int8, int num_sms, int m
   const int avail = max_smem - K * 4 - kReserve;
   int room = avail / buf_bytes;
   room = room > kMaxBuf ? kMaxBuf : room;
-  // nbuf = nwarps * depth: among 8, 6 or 4 warps the most slots that fit
+  // nbuf = nwarps * depth: among 8 to 4 warps the most slots that fit
   // (then the most warps); with room for fewer than four buffers, one each
   int best_w = room, best_n = room;
   if (room >= 4) {
     best_n = 0;
-    for (int w : {8, 6, 4}) {
+    for (int w : {8, 7, 6, 5, 4}) {
       const int n = (room / w) * w;
       if (n > best_n) {
         best_w = w;
