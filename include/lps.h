@@ -74,6 +74,32 @@ int stage_plan_fence(const lps_stage_plan* plan, int* fence, int cap);
 /* The stage that owns layer il (memra_engine::pp, stage_of); LPS_EINVAL if il is out of range. */
 int stage_of(const lps_stage_plan* plan, int il);
 
+/* Memory-balancing cuts (ninfer pipeline-stages.md, "How it works":
+ * solve_stage_plan -- the largest capacity every stage can hold, then the
+ * least-full stage; when nothing fits, the layers dealt evenly). Stage s
+ * holding layers [i, j) at a capacity of P units (a unit is one context
+ * position of the per-stage KV cache) uses
+ *     stage_fixed[s] + sum(layer_bytes[i..j)) + P * sum(layer_unit_bytes[i..j))
+ * bytes and must stay within stage_free[s]. The cuts returned give the
+ * largest P in [0, max_units] over all contiguous plans with every stage
+ * non-empty; among those, the smallest fullest-stage fraction
+ * max_s(used_s / stage_free[s]) (compared exactly); among those, the
+ * lexicographically smallest cuts. Host only, exact (not a heuristic).
+ *   layer_bytes, layer_unit_bytes  host uint64[n_layers]
+ *   stage_free   host uint64[n_stages], each > 0 (stages sharing one device
+ *                split its free bytes between them)
+ *   stage_fixed  host uint64[n_stages] or NULL (zeros): bytes a stage needs
+ *                beyond its layers (workspace; the embedding on stage 0, the
+ *                final norm, LM head and logits on the last stage)
+ *   cuts_out     host int[n_stages - 1], for stage_plan_create
+ *   units_out    the capacity P, or -1 when no plan fits even at P = 0 (the
+ *                cuts are then the even split of stage_plan_create)
+ * LPS_EINVAL for NULL arguments, n_stages outside [1, n_layers], max_units < 0
+ * or a stage with no free bytes. */
+int stage_plan_solve(int n_layers, int n_stages, const uint64_t* layer_bytes, const uint64_t* layer_unit_bytes,
+                     const uint64_t* stage_free, const uint64_t* stage_fixed, int64_t max_units, int* cuts_out,
+                     int64_t* units_out);
+
 /* ---- model description and weights ------------------------------------- */
 #define LPS_WEIGHT_BF16 0          /* bf16 weights */
 #define LPS_WEIGHT_INT8_ROWSCALE 1 /* int8 weights with one fp32 scale per output row: w = q * s_row */
@@ -133,6 +159,18 @@ typedef struct lps_model_weights {
   lps_matrix lm_head;              /* [vocab, n_embd] untied head (last stage) */
   const lps_layer_weights* layers; /* [n_layers] */
 } lps_model_weights;
+
+/* The byte model stage_plan_solve takes, for a model bound with this
+ * library: layer_bytes[l] = the weights of layer l (QKV, o, gate, up, down,
+ * int8 row scales, both norms); layer_unit_bytes[l] = its KV cache per context
+ * position (K and V rows of every sequence, bf16); first_stage_bytes = the
+ * embedding; last_stage_bytes = the LM head, final norm and logits buffers;
+ * every_stage_bytes = a stage's activations, attention partials (one per 64
+ * positions, a bound), RoPE table and boundary slots at desc->max_ctx -- a
+ * close estimate, not the exact allocation. Host arrays of n_layers entries.
+ * LPS_EINVAL for NULL arguments or a bad shape. */
+int model_stage_bytes(const lps_model_desc* desc, uint64_t* layer_bytes, uint64_t* layer_unit_bytes,
+                      uint64_t* first_stage_bytes, uint64_t* last_stage_bytes, uint64_t* every_stage_bytes);
 
 /* Optional runtime hooks. alloc/free route every device allocation of the
  * model (weights, caches, scratch, slots) to the caller, e.g. PyTorch's

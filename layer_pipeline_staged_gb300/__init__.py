@@ -24,8 +24,8 @@ from ._capi import (KERNELS, LPS_EBUSY, LPS_ECUDA, LPS_EINVAL, LPS_ENOMEM, LPS_E
                     LPS_OK)
 
 __all__ = ["LpsError", "StagePlan", "Model", "Pending", "stage_plan_create", "stage_plan_from_counts",
-           "model_bind", "decode_step", "decode_step_deferred", "pending_wait", "pending_free",
-           "decode_step_device", "load"]
+           "stage_plan_solve", "model_stage_bytes", "model_bind", "decode_step", "decode_step_deferred",
+           "pending_wait", "pending_free", "decode_step_device", "load"]
 
 
 class LpsError(RuntimeError):
@@ -288,6 +288,37 @@ def stage_plan_create(n_layers: int, cuts=None, n_stages: int | None = None) -> 
 
 def stage_plan_from_counts(counts) -> StagePlan:
     return StagePlan(counts=counts)
+
+
+def stage_plan_solve(layer_bytes, layer_unit_bytes, stage_free, stage_fixed=None, max_units: int = 1 << 40):
+    """Memory-balancing cuts (the C ABI's stage_plan_solve): returns (cuts, units), units = -1
+    when nothing fits (the cuts are then the even split)."""
+    lb = np.ascontiguousarray(layer_bytes, np.uint64)
+    lu = np.ascontiguousarray(layer_unit_bytes, np.uint64)
+    sf = np.ascontiguousarray(stage_free, np.uint64)
+    if len(lu) != len(lb):
+        raise ValueError("layer_bytes and layer_unit_bytes differ in length")
+    sx = None if stage_fixed is None else np.ascontiguousarray(stage_fixed, np.uint64)
+    if sx is not None and len(sx) != len(sf):
+        raise ValueError("stage_fixed and stage_free differ in length")
+    cuts = np.zeros(max(len(sf) - 1, 1), np.int32)
+    units = ctypes.c_int64()
+    _check(load().stage_plan_solve(len(lb), len(sf), _ptr(lb), _ptr(lu), _ptr(sf), _ptr(sx), int(max_units),
+                                   _ptr(cuts), ctypes.byref(units)))
+    return [int(c) for c in cuts[:len(sf) - 1]], int(units.value)
+
+
+def model_stage_bytes(desc: dict) -> dict:
+    """The byte model of a bound model (the C ABI's model_stage_bytes): per-layer weight and
+    per-position KV bytes, and the embedding / head / per-stage workspace constants."""
+    d = _capi.ModelDesc(**desc)
+    lb = np.zeros(d.n_layers, np.uint64)
+    lu = np.zeros(d.n_layers, np.uint64)
+    first, last, every = ctypes.c_uint64(), ctypes.c_uint64(), ctypes.c_uint64()
+    _check(load().model_stage_bytes(ctypes.byref(d), _ptr(lb), _ptr(lu), ctypes.byref(first), ctypes.byref(last),
+                                    ctypes.byref(every)))
+    return {"layer_bytes": lb, "layer_unit_bytes": lu, "first_stage_bytes": int(first.value),
+            "last_stage_bytes": int(last.value), "every_stage_bytes": int(every.value)}
 
 
 def model_bind(plan: StagePlan, desc: dict, weights: dict, device: int = 0, use_torch: bool | None = None) -> Model:

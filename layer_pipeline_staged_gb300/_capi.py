@@ -32,6 +32,7 @@ EXPORTS = (
     "last_error_string", "model_stats", "model_kv_export", "model_kv_import", "model_attn_out",
     "model_time_kernel", "model_kernel_time", "model_set_serial_steps", "attention_decode_noalloc", "attention_decode_noalloc_error",
     "attention_decode_noalloc_scratch_bytes", "model_trace_enable", "model_trace_read", "model_trace_disable",
+    "stage_plan_solve", "model_stage_bytes",
 )
 
 
@@ -119,6 +120,9 @@ def load(path: str = LIB_PATH):
         "attention_decode_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, i, vp, vp]),
         "attention_decode_noalloc_error": (ctypes.c_char_p, []),
         "attention_decode_noalloc_scratch_bytes": (ctypes.c_longlong, [i, i, i, i, i]),
+        "stage_plan_solve": (i, [i, i, vp, vp, vp, vp, ctypes.c_int64, vp, ctypes.POINTER(ctypes.c_int64)]),
+        "model_stage_bytes": (i, [ctypes.POINTER(ModelDesc), vp, vp, ctypes.POINTER(ctypes.c_uint64),
+                                  ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)

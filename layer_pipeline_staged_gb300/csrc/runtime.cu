@@ -56,6 +56,11 @@ int cuda_fail(const char* fn, const char* what, cudaError_t e) {
 
 }  // namespace
 
+namespace lps {
+// The thread's last error, for host code in other files (the stage solver).
+int host_fail(int code, const char* fn, const std::string& why) { return fail(code, fn, why); }
+}  // namespace lps
+
 // ---------------------------------------------------------------------------
 // stage plan
 // ---------------------------------------------------------------------------
