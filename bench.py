@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fill", default="synthetic", choices=["synthetic", "decode"])
     ap.add_argument("--serial", action="store_true", help="no overlap between consecutive steps' stages")
+    ap.add_argument("--verify", type=int, default=0,
+                    help="speculative-verify rows: each step verifies this many consecutive positions of one "
+                         "sequence (LPS_FLAG_VERIFY, batch = rows); 0 = ordinary decode")
     ap.add_argument("--layers", type=int, default=None,
                     help="profiling only: keep the first N layers (a smaller case for ncu); not a bench number")
     return ap.parse_args()
@@ -90,11 +93,6 @@ def kernel_bytes(cfg, kind: str, pos: int) -> int:
         kv = B * cfg.kv_heads * cfg.head_dim * 2 * 2 * (pos + 1)  # K and V rows [0, pos], bf16
         return kv + 2 * B * qw * 4  # q in, attention output out
     raise ValueError(kind)
-
-
-def dominant_kernel(cfg, pos: int) -> str:
-    """The kernel family that moves the most bytes per step (one launch per layer each)."""
-    return max(("gateup", "attn"), key=lambda k: kernel_bytes(cfg, k, pos))
 
 
 def kernel_traffic(kind: str, cfg_name: str):
@@ -237,6 +235,11 @@ def main():
         n = min(len(cfg.fence) - 1, args.layers)
         cfg = cfg.replace(n_layers=args.layers, cuts=tuple(s * args.layers // n for s in range(1, n)))
     ctx = args.ctx if args.ctx is not None else cfg.ctx
+    M = args.verify  # verify rows per step (one sequence), 0 = ordinary decode
+    if M:
+        if args.impl == "reference" or os.environ.get("WORLD_SIZE", "1") != "1":
+            raise SystemExit("--verify runs the GPU arm on one GPU only")
+        cfg = cfg.replace(name=f"{cfg.name}_verify{M}", batch=M)
     if args.impl == "reference":
         run_reference(args, cfg, ctx)
         return
@@ -258,22 +261,24 @@ def main():
     lps_build.build()
 
     K, W = args.steps, args.warmup
-    max_ctx = ctx + K
+    adv = M or 1  # positions a step advances
+    max_ctx = ctx + K * adv
     w = synth.make_weights(cfg)
     desc = dict(n_layers=cfg.n_layers, n_embd=cfg.n_embd, n_q_heads=cfg.q_heads, n_kv_heads=cfg.kv_heads,
                 head_dim=cfg.head_dim, ffn=cfg.ffn, vocab=cfg.vocab,
                 weight_dtype=1 if cfg.weight_dtype == "int8" else 0, kv_dtype=0, max_ctx=max_ctx,
                 batch=cfg.batch, pending_depth=4, rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps,
-                flags=lps.LPS_FLAG_SERIAL_STEPS if args.serial else 0)
+                flags=(lps.LPS_FLAG_SERIAL_STEPS if args.serial else 0) | (lps.LPS_FLAG_VERIFY if M else 0))
     plan = lps.stage_plan_create(cfg.n_layers, cuts=list(cfg.cuts))
     model = lps.model_bind(plan, desc, w, device=local)
     B, V = cfg.batch, cfg.vocab
     toks = synth.make_tokens(cfg, W + K)
-    start = ctx - W
+    start = ctx - W * adv
+    seqs = 1 if M else B  # sequences with a cache of their own
     # context rows [0, start): synthetic cache contents, or teacher-forced decode steps
     if args.fill == "synthetic" and start > 0:
         for l in range(cfg.n_layers):
-            for b in range(B):
+            for b in range(seqs):
                 k = synth.uniform_bf16(cfg.seed_t + 5, 2 * (l * B + b), (cfg.kv_heads, max_ctx, cfg.head_dim))
                 v = synth.uniform_bf16(cfg.seed_t + 5, 2 * (l * B + b) + 1, (cfg.kv_heads, max_ctx, cfg.head_dim))
                 model.kv_import(l, b, k, v, start)
@@ -281,7 +286,7 @@ def main():
         ftoks = synth.make_tokens(cfg, start, seed=cfg.seed_t + 9)
         tdev = torch.tensor(ftoks, dtype=torch.int32, device="cuda")
         scratch = torch.empty((B, V), dtype=torch.float32, device="cuda")
-        for t in range(start):
+        for t in range(0, start, adv):
             model.decode_step_device(tdev[t].data_ptr(), t, scratch.data_ptr())
         model.synchronize()
 
@@ -292,11 +297,11 @@ def main():
 
     def device_pass(first_pos):
         for i in range(K):
-            model.decode_step_device(tok_dev[W + i].data_ptr(), first_pos + i, logits_dev.data_ptr())
+            model.decode_step_device(tok_dev[W + i].data_ptr(), first_pos + i * adv, logits_dev.data_ptr())
 
     # warm-up steps at positions start .. ctx-1
     for i in range(W):
-        model.decode_step_device(tok_dev[i].data_ptr(), start + i, logits_dev.data_ptr())
+        model.decode_step_device(tok_dev[i].data_ptr(), start + i * adv, logits_dev.data_ptr())
     model.synchronize()
 
     def barrier():
@@ -327,7 +332,7 @@ def main():
         t0 = time.perf_counter()
         pend = []
         for i in range(K):
-            pend.append(model.decode_step_deferred(toks[W + i], ctx + i))
+            pend.append(model.decode_step_deferred(toks[W + i], ctx + i * adv))
             if len(pend) == depth:
                 p = pend.pop(0)
                 p.wait(out=host_logits)
@@ -341,7 +346,12 @@ def main():
         # ---- the dominant kernel family timed live with CUDA events around each launch on its
         # stage stream (same steps again), stages serialized so that no other stage's kernels
         # run beside it
-        dom = dominant_kernel(cfg, ctx + K // 2)
+        # verify rows launch the attention once per row (batch 1 each)
+        attn_cfg = cfg.replace(batch=1) if M else cfg
+        pos_mid = ctx + (K // 2) * adv
+        per_launch = {k: kernel_bytes(attn_cfg if k == "attn" else cfg, k, pos_mid) for k in ("gateup", "attn")}
+        per_step = {k: per_launch[k] * (M if (M and k == "attn") else 1) for k in per_launch}
+        dom = max(per_step, key=per_step.get)
         if plan.n_stages > 1:
             model.set_serial_steps(True)
         model.time_kernel(dom, True)
@@ -357,10 +367,16 @@ def main():
         elapsed_ms, e2e_s = float(t[0]), float(t[1])
     n = world
     tok_s = n * B * K / (elapsed_ms / 1e3)
-    step_bytes = [cfg.step_bytes(ctx + i) for i in range(K)]
+    if M:
+        # weights once per step; each verify row reads its own rows [0, pos + j]
+        one = cfg.replace(batch=1)
+        step_bytes = [one.step_bytes(ctx + i * M) + sum(one.step_bytes(ctx + i * M + j) - one.weight_bytes()
+                                                         for j in range(1, M)) for i in range(K)]
+    else:
+        step_bytes = [cfg.step_bytes(ctx + i) for i in range(K)]
     hbm_gbs = sum(step_bytes) / (elapsed_ms / 1e3) / 1e9
     peaks, peak_src = measured_peaks()
-    dom_bytes = kernel_bytes(cfg, dom, ctx + K // 2)
+    dom_bytes = per_launch[dom]
     dom_avg_s = dom_ms / 1e3 / max(dom_n, 1)
     achieved = dom_bytes / dom_avg_s / 1e9
     wl = workload_name(cfg, ctx, K)
@@ -369,7 +385,9 @@ def main():
         cpu = cpu_baseline(cfg, w, ctx, args.cpu_seconds)
     clocks = clk.summary()
     line = {
-        "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": n, "steps": K, "warmup": W,
+        "metric": METRIC if not M else f"speculative-verify tokens/s ({M} consecutive positions of one sequence "
+                                          "per step) and achieved HBM GB/s, 1xGB300",
+        "value": tok_s, "unit": "tokens/s", "n_gpus": n, "steps": K, "warmup": W,
         "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": dtype_of(cfg), "data": "synthetic",
         "config": {"workload": wl, "l2": "inputs larger than L2 (every step streams all weights from HBM)",
@@ -379,7 +397,7 @@ def main():
         "hbm_gbs": hbm_gbs, "hbm_frac_of_8tbs": hbm_gbs / NOMINAL_HBM_GBS,
         "hbm_frac_of_measured": hbm_gbs / peaks["hbm_gbs"],
         "bytes_per_step": sum(step_bytes) / K,
-        "roofline": {"kernel": KERNEL_NAMES[dom] + f" ({100 * dom_bytes * cfg.n_layers / (sum(step_bytes) / K):.0f}% "
+        "roofline": {"kernel": KERNEL_NAMES[dom] + f" ({100 * per_step[dom] * cfg.n_layers / (sum(step_bytes) / K):.0f}% "
                                "of step bytes; launches timed with stages serialized)", "bound": "hbm",
                      "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"

@@ -109,6 +109,13 @@ int stage_plan_solve(int n_layers, int n_stages, const uint64_t* layer_bytes, co
                                       device-to-device copies (memra_engine::pp, pp2_streams_off) */
 #define LPS_FLAG_KEEP_ATTN_OUT 2u  /* keep each layer's attention output of the latest step
                                       readable through model_attn_out (debug) */
+#define LPS_FLAG_VERIFY 8u         /* speculative-verify rows (memra_engine::pp, spec_pp_on: the verify
+                                      forward takes the stage split): the batch's B rows are B
+                                      consecutive positions of ONE sequence -- pos[b] == pos[0] + b --
+                                      with one KV cache; row b writes cache row pos[b] and attends
+                                      [0, pos[b]], so it sees the rows before it in the same step,
+                                      and the step returns the logits of every row. The cache calls
+                                      (model_kv_export/import) take sequence 0 only. */
 #define LPS_FLAG_SERIAL_STEPS 4u   /* make stage 0 of step t+1 also wait for the last stage of step t.
                                       By default stages of consecutive steps overlap, bounded
                                       only by the slot events (tokens t+1.. keep running while

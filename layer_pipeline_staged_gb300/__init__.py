@@ -20,7 +20,8 @@ import numpy as np
 
 from . import _capi
 from ._capi import (KERNELS, LPS_EBUSY, LPS_ECUDA, LPS_EINVAL, LPS_ENOMEM, LPS_ETIMEDOUT,  # noqa: F401
-                    LPS_FLAG_KEEP_ATTN_OUT, LPS_FLAG_SERIAL_STEPS, LPS_FLAG_SINGLE_STREAM, LPS_NOALLOC_SCRATCH_BYTES,
+                    LPS_FLAG_KEEP_ATTN_OUT, LPS_FLAG_SERIAL_STEPS, LPS_FLAG_SINGLE_STREAM, LPS_FLAG_VERIFY,
+                    LPS_NOALLOC_SCRATCH_BYTES,
                     LPS_OK)
 
 __all__ = ["LpsError", "StagePlan", "Model", "Pending", "stage_plan_create", "stage_plan_from_counts",
@@ -180,20 +181,26 @@ class Model:
     def _vec(self, x) -> np.ndarray:
         return np.ascontiguousarray(np.broadcast_to(np.asarray(x, dtype=np.int32), (self.B,)))
 
+    def _pos(self, pos) -> np.ndarray:
+        # verify rows (LPS_FLAG_VERIFY): a scalar is the first row's position
+        if self.desc.flags & _capi.LPS_FLAG_VERIFY and np.ndim(pos) == 0:
+            return np.ascontiguousarray(int(pos) + np.arange(self.B, dtype=np.int32))
+        return self._vec(pos)
+
     def decode_step(self, tokens, pos, out: np.ndarray | None = None) -> np.ndarray:
-        t, p = self._vec(tokens), self._vec(pos)
+        t, p = self._vec(tokens), self._pos(pos)
         out = np.empty((self.B, self.V), np.float32) if out is None else out
         _check(load().decode_step(self.h, _ptr(t), _ptr(p), _ptr(out)))
         return out
 
     def decode_step_deferred(self, tokens, pos) -> "Pending":
-        t, p = self._vec(tokens), self._vec(pos)
+        t, p = self._vec(tokens), self._pos(pos)
         h = ctypes.c_void_p()
         _check(load().decode_step_deferred(self.h, _ptr(t), _ptr(p), ctypes.byref(h)))
         return Pending(self, h)
 
     def decode_step_device(self, tokens_dev_ptr: int, pos, logits_dev_ptr: int):
-        p = self._vec(pos)
+        p = self._pos(pos)
         _check(load().decode_step_device(self.h, ctypes.c_void_p(tokens_dev_ptr), _ptr(p),
                                          ctypes.c_void_p(logits_dev_ptr)))
 

@@ -21,6 +21,7 @@ LPS_NOALLOC_SCRATCH_BYTES = 8 << 20
 LPS_FLAG_SINGLE_STREAM = 1
 LPS_FLAG_KEEP_ATTN_OUT = 2
 LPS_FLAG_SERIAL_STEPS = 4
+LPS_FLAG_VERIFY = 8
 
 KERNELS = {"qkv": 0, "attn": 1, "oproj": 2, "gateup": 3, "down": 4, "head": 5, "embed": 6}
 

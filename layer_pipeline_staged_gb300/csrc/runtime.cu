@@ -208,6 +208,7 @@ struct lps_model {
   bool int8 = false;
   bool single = false;
   bool skinny = false;  // batch > 1: tensor-core skinny GEMMs on the tiled weight layout
+  bool verify = false;  // LPS_FLAG_VERIFY: the batch rows are consecutive positions of one sequence
   lps_alloc_fn alloc = nullptr;
   lps_free_fn free_fn = nullptr;
   void* alloc_ctx = nullptr;
@@ -606,8 +607,10 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
     m->own_rb = true;
   }
 
-  // chunking of the attention partials, sized for the longest context
-  m->attn_max_chunks = attn_max_chunks(hd, nkv, B, d.max_ctx, m->num_sms);
+  // chunking of the attention partials, sized for the longest context (the
+  // verify arm attends one row per launch)
+  m->verify = (d.flags & LPS_FLAG_VERIFY) != 0;
+  m->attn_max_chunks = attn_max_chunks(hd, nkv, m->verify ? 1 : B, d.max_ctx, m->num_sms);
 
   // rope table (cos, sin) of angle pos * theta^(-2i/hd), computed in double
   std::vector<float2> rope(static_cast<size_t>(d.max_ctx) * half);
@@ -623,7 +626,8 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
   if (!m->status_dev || !m->status_host) return bail(LPS_ENOMEM, "status word allocation failed");
   if (cudaMemset(m->status_dev, 0, sizeof(int)) != cudaSuccess) return bail(LPS_ECUDA, "cudaMemset failed");
 
-  const size_t kv_elems = static_cast<size_t>(B) * nkv * d.max_ctx * hd;
+  const int seqs = m->verify ? 1 : B;  // sequences with a cache of their own
+  const size_t kv_elems = static_cast<size_t>(seqs) * nkv * d.max_ctx * hd;
   std::string why;
   // batch > 1: a row-major staging buffer on the device for retiling (the largest matrix)
   void* temp = nullptr;
@@ -727,8 +731,8 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
       D.kc = static_cast<__nv_bfloat16*>(dev_alloc(m, kv_elems * 2));
       D.vc = static_cast<__nv_bfloat16*>(dev_alloc(m, kv_elems * 2));
       if (!D.attn_norm || !D.ffn_norm || !D.kc || !D.vc) return bail(LPS_ENOMEM, "KV cache allocation failed");
-      if (!make_kv_map(&D.tmap_k, D.kc, hd, static_cast<unsigned long long>(B) * nkv * d.max_ctx, attn_sub_tile(hd)) ||
-          !make_kv_map(&D.tmap_v, D.vc, hd, static_cast<unsigned long long>(B) * nkv * d.max_ctx, attn_sub_tile(hd)))
+      if (!make_kv_map(&D.tmap_k, D.kc, hd, static_cast<unsigned long long>(seqs) * nkv * d.max_ctx, attn_sub_tile(hd)) ||
+          !make_kv_map(&D.tmap_v, D.vc, hd, static_cast<unsigned long long>(seqs) * nkv * d.max_ctx, attn_sub_tile(hd)))
         return bail(LPS_ECUDA, "cuTensorMapEncodeTiled failed for the KV cache");
       up.put(D.attn_norm, L.attn_norm, sizeof(float) * E);
       up.put(D.ffn_norm, L.ffn_norm, sizeof(float) * E);
@@ -800,7 +804,7 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
   }
   e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return bail(LPS_ECUDA, std::string("bind: ") + cudaGetErrorString(e));
-  m->filled.assign(B, 0);
+  m->filled.assign(seqs, 0);
   m->stats.n_stages = N;
   for (int i = 0; i <= N && i < 17; ++i) m->stats.fence[i] = m->fence[i];
   *out = m;
@@ -828,9 +832,15 @@ int check_step(lps_model* m, const int32_t* tokens, const int32_t* pos, bool tok
       return fail(LPS_EINVAL, FN, "token " + std::to_string(b) + " out of [0, vocab)");
     if (pos[b] < 0 || pos[b] >= m->d.max_ctx)
       return fail(LPS_EINVAL, FN, "pos " + std::to_string(b) + " out of [0, max_ctx)");
-    if (pos[b] > m->filled[b])
+    if (m->verify) {
+      // the rows are consecutive positions of the one sequence
+      if (pos[b] != pos[0] + b) return fail(LPS_EINVAL, FN, "verify rows need pos[b] == pos[0] + b");
+    } else if (pos[b] > m->filled[b]) {
       return fail(LPS_EINVAL, FN, "pos " + std::to_string(b) + " skips unwritten cache rows (pos > filled)");
+    }
   }
+  if (m->verify && pos[0] > m->filled[0])
+    return fail(LPS_EINVAL, FN, "pos 0 skips unwritten cache rows (pos > filled)");
   return LPS_OK;
 }
 
@@ -847,7 +857,8 @@ SkinnyParams skinny_params(const lps_model* m, const void* w, const float* wscal
   p.nkv = m->d.n_kv_heads;
   p.hd = m->d.head_dim;
   p.max_ctx = m->d.max_ctx;
-  p.kv_stride = static_cast<size_t>(m->d.n_kv_heads) * m->d.max_ctx * m->d.head_dim;
+  // verify rows all write the one sequence's cache (row pos[b] each)
+  p.kv_stride = m->verify ? 0 : static_cast<size_t>(m->d.n_kv_heads) * m->d.max_ctx * m->d.head_dim;
   for (int b = 0; b < m->d.batch; ++b) p.pos[b] = pos[b];
   p.status = m->status_dev;
   return p;
@@ -945,8 +956,9 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
         p.gain = L.attn_norm;
         p.eps = d.rms_eps;
         p.out = S.q + static_cast<size_t>(b) * qw;
-        p.kc = L.kc + static_cast<size_t>(b) * nkv * d.max_ctx * hd;
-        p.vc = L.vc + static_cast<size_t>(b) * nkv * d.max_ctx * hd;
+        const size_t seq = m->verify ? 0 : static_cast<size_t>(b);
+        p.kc = L.kc + seq * nkv * d.max_ctx * hd;
+        p.vc = L.vc + seq * nkv * d.max_ctx * hd;
         p.rope = S.rope + static_cast<size_t>(pos[b]) * half;
         p.nq = nq;
         p.nkv = nkv;
@@ -977,7 +989,22 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
         ap.scale = 1.0f / std::sqrt(static_cast<float>(hd));
         ap.early_dependents = m->skinny ? 0 : 1;  // the GEMV o-proj follows
         ap.status = m->status_dev;
-        LAUNCH(LPS_KERNEL_ATTN, cs, ap, launch_attention(ap, B, max_pos, cs, pdl));
+        if (!m->verify) {
+          LAUNCH(LPS_KERNEL_ATTN, cs, ap, launch_attention(ap, B, max_pos, cs, pdl));
+        } else {
+          // verify rows share the one cache: one launch per row b, attending
+          // [0, pos[b]] (rows pos[0]..pos[b] were written by this step's QKV)
+          for (int b = 0; b < B; ++b) {
+            AttnParams ab = ap;
+            ab.q = S.q + static_cast<size_t>(b) * qw;
+            ab.out = o_buf + static_cast<size_t>(b) * qw;
+            ab.part = S.part + static_cast<size_t>(b) * nq * m->attn_max_chunks * (hd + 4);
+            ab.counter = S.counter + static_cast<size_t>(b) * nkv;
+            ab.pos[0] = pos[b];
+            ab.chunk = attn_chunk(hd, nkv, 1, pos[b], m->num_sms);
+            LAUNCH(LPS_KERNEL_ATTN, cs, ab, launch_attention(ab, 1, pos[b], cs, pdl));
+          }
+        }
       }
       // o-proj + residual (the first layer of a later stage reads the boundary slot)
       if (m->skinny) {
@@ -1103,7 +1130,10 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
     if (N > 1 && !m->single && !m->overlap) CK(cudaEventRecord(m->ev_step, cs), "record step event");
   }
 #undef LAUNCH
-  for (int b = 0; b < B; ++b) m->filled[b] = pos[b] + 1;
+  if (m->verify)
+    m->filled[0] = pos[B - 1] + 1;
+  else
+    for (int b = 0; b < B; ++b) m->filled[b] = pos[b] + 1;
   ++m->step_count;
   ++m->stats.steps;
   m->stats.kernel_launches += launches;
@@ -1266,7 +1296,7 @@ extern "C" int model_stats(const lps_model* m, lps_stats* out) {
 namespace {
 int kv_locate(const lps_model* m, int layer, int b, size_t bytes, const LayerDev** L, cudaStream_t* stream,
               const char* FN) {
-  if (!m || layer < 0 || layer >= m->d.n_layers || b < 0 || b >= m->d.batch)
+  if (!m || layer < 0 || layer >= m->d.n_layers || b < 0 || b >= (m->verify ? 1 : m->d.batch))
     return fail(LPS_EINVAL, FN, "bad model, layer or sequence");
   const size_t want = 4ull * m->d.n_kv_heads * m->d.max_ctx * m->d.head_dim;
   if (bytes != want) return fail(LPS_EINVAL, FN, "bytes must be 4 * nkv * max_ctx * hd");
