@@ -18,69 +18,119 @@ import layer_pipeline_staged_gb300 as lps
 from oracle import stage_solver as orc
 
 # ---------------------------------------------------------------------------
-# pins: the oracle against hand-worked cases
+# pins: the oracle against hand-worked cases (each takes the oracle module, so
+# that the mutant test below can run them on planted mistakes too)
 # ---------------------------------------------------------------------------
 
 
-def test_pin_one_stage_closed_form():
+def pin_one_stage_closed_form(mod):
     # one stage: P = floor((free - fixed - sum W) / sum U) = floor((1000 - 100 - 60) / 7) = 120
-    assert orc.solve([10, 20, 30], [1, 2, 4], [1000], [100]) == ([], 120)
+    assert mod.solve([10, 20, 30], [1, 2, 4], [1000], [100]) == ([], 120)
 
 
-def test_pin_even_layers_even_split():
+def pin_even_layers_even_split(mod):
     # 4 layers of 10 B + 1 B per unit, two stages of 100 B: the 2/2 split gives
     # 20 + 2P <= 100 -> P = 40; 1/3 gives 30 + 3P <= 100 -> P = 23
-    assert orc.solve([10] * 4, [1] * 4, [100, 100]) == ([2], 40)
+    assert mod.solve([10] * 4, [1] * 4, [100, 100]) == ([2], 40)
 
 
-def test_pin_twice_the_memory_gets_more_layers():
+def pin_twice_the_memory_gets_more_layers(mod):
     # 6 layers of 10 B + 1 B per unit; stage 1 has twice the memory.
     # cuts 2: min((100-20)/2, (200-40)/4) = min(40, 40) = 40; cuts 3: min(70/3=23, 170/3=56) = 23;
     # cuts 1: min(90, 150/5=30) = 30 -> cut 2, the bigger stage holds 4 of 6
-    cuts, units = orc.solve([10] * 6, [1] * 6, [100, 200])
+    cuts, units = mod.solve([10] * 6, [1] * 6, [100, 200])
     assert (cuts, units) == ([2], 40)
     assert 6 - cuts[0] > cuts[0]
 
 
-def test_pin_head_stage_gets_fewer_layers():
+def pin_head_stage_gets_fewer_layers(mod):
     # 8 layers of 10 B + 1 B per unit, two stages of 100 B, the last one also holding a
     # 30 B head. Cut c: stage 0 allows (100 - 10c) / c units, stage 1 (10c - 10) / (8 - c).
     # c = 4: min(15, 7) = 7; c = 5: min(10, 13) = 10; c = 6: min(6, 25) = 6 -> c = 5,
     # the head stage holds 3 of the 8 layers
-    cuts, units = orc.solve([10] * 8, [1] * 8, [100, 100], [0, 30])
-    assert (cuts, units) == ([5], 10)
+    assert mod.solve([10] * 8, [1] * 8, [100, 100], [0, 30]) == ([5], 10)
 
 
-def test_pin_nothing_fits_deals_evenly():
+def pin_nothing_fits_deals_evenly(mod):
     # 5 layers of 10 B over two stages of 15 B: some stage holds at least three layers
     # (30 B), so nothing fits; the even split of 5 layers over 2 stages is cut 1 * 5 // 2 = 2
-    assert orc.solve([10] * 5, [0] * 5, [15, 15]) == ([2], -1)
+    assert mod.solve([10] * 5, [0] * 5, [15, 15]) == ([2], -1)
+    # 7 layers over 3 stages: cuts 7 // 3 = 2 and 14 // 3 = 4
+    assert mod.solve([10] * 7, [0] * 7, [5, 5, 5]) == ([2, 4], -1)
 
 
-def test_pin_small_stage_between_large_layers():
+def pin_small_stage_between_large_layers(mod):
     # layers 1, 1, 9, 1 over stages of 2, 1, 10 bytes: the only plan that fits
     # gives stage 1 exactly layer 1 (cuts 1, 2); stage 0 taking both small
     # layers would leave stage 1 the 9-byte layer
-    assert orc.solve([1, 1, 9, 1], [0, 0, 0, 0], [2, 1, 10], max_units=50) == ([1, 2], 50)
+    assert mod.solve([1, 1, 9, 1], [0, 0, 0, 0], [2, 1, 10], max_units=50) == ([1, 2], 50)
 
 
-def test_pin_fraction_breaks_capacity_ties():
+def pin_fraction_breaks_capacity_ties(mod):
     # zero unit bytes: every fitting plan has capacity max_units; the fullest
     # stage decides. layers 5, 5, 5, 5, stages 40 and 10: cuts 3 -> max(15/40, 5/10) = 1/2,
     # cuts 2 -> max(10/40, 10/10) = 1 (fits exactly), cuts 1 -> 15/10 does not fit
-    assert orc.solve([5] * 4, [0] * 4, [40, 10], max_units=9) == ([3], 9)
+    assert mod.solve([5] * 4, [0] * 4, [40, 10], max_units=9) == ([3], 9)
 
 
-def test_pin_lexicographic_among_equals():
+def pin_fraction_counts_the_units(mod):
+    # the fullest stage is judged at the solved capacity, units included: layers 10, 10, 10,
+    # unit bytes 0, 0, 5, stages of 100 and 100, max 4 units. Cuts 1: stage 1 holds 20 + 4*5 = 40;
+    # cuts 2: stage 0 holds 20, stage 1 holds 10 + 20 = 30 -> max(20/100, 30/100) beats
+    # max(10/100, 40/100): cuts 2 (without the units cuts 1 and 2 would both be 20/100)
+    assert mod.solve([10, 10, 10], [0, 0, 5], [100, 100], max_units=4) == ([2], 4)
+
+
+def pin_lexicographic_among_equals(mod):
     # two identical stages, 3 equal layers, no unit bytes: cuts 1 and 2 are mirror
     # images with the same fullest fraction (20/30); the first in lexicographic order wins
-    assert orc.solve([10] * 3, [0] * 3, [30, 30], max_units=5) == ([1], 5)
+    assert mod.solve([10] * 3, [0] * 3, [30, 30], max_units=5) == ([1], 5)
 
 
-def test_pin_capacity_capped():
-    assert orc.stage_capacity(100, 0, 0, 0, 77) == 77
-    assert orc.stage_capacity(100, 10, 20, 7, 1000) == 10
-    assert orc.stage_capacity(100, 90, 20, 1, 1000) == -1
+def pin_capacity_capped(mod):
+    assert mod.stage_capacity(100, 0, 0, 0, 77) == 77
+    assert mod.stage_capacity(100, 10, 20, 7, 1000) == 10
+    assert mod.stage_capacity(100, 90, 20, 1, 1000) == -1
+    assert mod.stage_capacity(100, 10, 20, 7, 5) == 5
+
+
+PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin(orc)
+
+
+# plausible mistakes planted in copies of the oracle: every one must fail a pin
+MUTANTS = {
+    "capacity_off_by_one": ("return min(max_units, room // unit)", "return min(max_units, room // unit + 1)"),
+    "fixed_bytes_ignored": ("room = free - fixed - weights", "room = free - weights"),
+    "capacity_not_capped": ("return min(max_units, room // unit)", "return room // unit"),
+    "one_layer_unit_bytes": ("u = sum(layer_unit_bytes[fence[s]:fence[s + 1]])", "u = layer_unit_bytes[fence[s]]"),
+    "plan_capacity_max": ("return min(caps)", "return max(caps)"),
+    "fullest_without_units": ("+ P * sum(layer_unit_bytes[fence[s]:fence[s + 1]])", ""),
+    "fraction_reversed": ("frac < best[1]", "frac > best[1]"),
+    "last_of_equals": ("(cap == best[0] and frac < best[1])", "(cap == best[0] and frac <= best[1])"),
+    "even_split_shifted": ("[s * L // N for s in range(1, N)]", "[(s * L + N - 1) // N for s in range(1, N)]"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name):
+    import types
+    old, new = MUTANTS[name]
+    src = open(orc.__file__).read()
+    assert src.count(old) == 1, f"mutant {name}: snippet not found once"
+    mod = types.ModuleType(f"stage_solver_{name}")
+    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), mod.__dict__)
+    caught = []
+    for pin in PINS:
+        try:
+            pin(mod)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches the mutant {name}"
 
 
 # ---------------------------------------------------------------------------
@@ -112,7 +162,8 @@ def test_library_matches_brute_force_on_random_cases():
 def test_library_matches_brute_force_on_pins():
     cases = [([10, 20, 30], [1, 2, 4], [1000], [100], 1 << 40), ([10] * 8, [1] * 8, [100, 100], [0, 30], 1 << 40),
              ([1, 1, 9, 1], [0] * 4, [2, 1, 10], None, 50), ([10] * 5, [0] * 5, [15, 15], None, 9),
-             ([5] * 4, [0] * 4, [40, 10], None, 9), ([10] * 3, [0] * 3, [30, 30], None, 5)]
+             ([5] * 4, [0] * 4, [40, 10], None, 9), ([10] * 3, [0] * 3, [30, 30], None, 5),
+             ([10, 10, 10], [0, 0, 5], [100, 100], None, 4), ([10] * 7, [0] * 7, [5, 5, 5], None, 3)]
     for lb, lu, free, fixed, mu in cases:
         assert lps.stage_plan_solve(lb, lu, free, fixed, mu) == orc.solve(lb, lu, free, fixed, mu)
 
