@@ -95,6 +95,22 @@ def kernel_bytes(cfg, kind: str, pos: int) -> int:
     raise ValueError(kind)
 
 
+def max_over_ranks(values, dist=None, device: str = "cuda") -> list:
+    """Each value's maximum over all ranks (a multi-rank job takes as long as its slowest
+    rank); the values themselves with one rank."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_rate(world: int, rows: int, steps: int, seconds: float) -> float:
+    """Whole-job throughput: the rows every rank processed in the slowest rank's time."""
+    return world * rows * steps / seconds
+
+
 def kernel_traffic(kind: str, cfg_name: str):
     """DRAM bytes per launch of a kernel family on a workload, from the committed ncu
     summary, if the kernel's sources still match the ones it was captured with."""
@@ -361,12 +377,9 @@ def main():
         if plan.n_stages > 1:
             model.set_serial_steps(args.serial)
 
-    if dist:
-        t = torch.tensor([elapsed_ms, e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms, e2e_s = float(t[0]), float(t[1])
+    elapsed_ms, e2e_s = max_over_ranks([elapsed_ms, e2e_s], dist)
     n = world
-    tok_s = n * B * K / (elapsed_ms / 1e3)
+    tok_s = job_rate(n, B, K, elapsed_ms / 1e3)
     if M:
         # weights once per step; each verify row reads its own rows [0, pos + j]
         one = cfg.replace(batch=1)
@@ -405,7 +418,7 @@ def main():
                      "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_us": dom_avg_s * 1e6,
                      "launches_timed": dom_n, "traffic": kernel_traffic(dom, cfg.name)},
         "cpu_baseline": cpu,
-        "e2e": {"value": n * B * K / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": B * 8,
+        "e2e": {"value": job_rate(n, B, K, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": B * 8,
                 "d2h_bytes_per_step": B * V * 4,
                 "how": "decode_step_deferred + pending_wait with host token ids and host logits, 4 steps in flight"},
         "gpu_launches": launches,
