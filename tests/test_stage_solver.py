@@ -159,6 +159,19 @@ def test_library_matches_brute_force_on_random_cases():
         assert got == want, (lb, lu, free, fixed, mu, got, want)
 
 
+def test_library_matches_brute_force_on_larger_cases():
+    # up to 14 layers over 5 stages (1001 plans each), layer sizes of two orders of magnitude
+    rng = random.Random(77)
+    for _ in range(150):
+        L = rng.randint(8, 14)
+        N = rng.randint(2, 5)
+        lb = [rng.choice([100, 150, 900, 1000, 1100]) for _ in range(L)]
+        lu = [rng.choice([1, 2, 3]) for _ in range(L)]
+        free = [rng.randint(sum(lb) // N, 2 * sum(lb) // N + 500) for _ in range(N)]
+        fixed = [rng.choice([0, 50, 400]) for _ in range(N)]
+        assert lps.stage_plan_solve(lb, lu, free, fixed, 10**6) == orc.solve(lb, lu, free, fixed, 10**6)
+
+
 def test_library_matches_brute_force_on_pins():
     cases = [([10, 20, 30], [1, 2, 4], [1000], [100], 1 << 40), ([10] * 8, [1] * 8, [100, 100], [0, 30], 1 << 40),
              ([1, 1, 9, 1], [0] * 4, [2, 1, 10], None, 50), ([10] * 5, [0] * 5, [15, 15], None, 9),
