@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fill", default="synthetic", choices=["synthetic", "decode"])
     ap.add_argument("--serial", action="store_true", help="no overlap between consecutive steps' stages")
+    ap.add_argument("--stages", type=int, default=0,
+                    help="even split into this many stages instead of the workload's own cuts (0 = the workload's)")
     ap.add_argument("--verify", type=int, default=0,
                     help="speculative-verify rows: each step verifies this many consecutive positions of one "
                          "sequence (LPS_FLAG_VERIFY, batch = rows); 0 = ordinary decode")
@@ -250,6 +252,9 @@ def main():
     if args.layers:
         n = min(len(cfg.fence) - 1, args.layers)
         cfg = cfg.replace(n_layers=args.layers, cuts=tuple(s * args.layers // n for s in range(1, n)))
+    if args.stages:
+        n = args.stages
+        cfg = cfg.replace(name=f"{cfg.name}_s{n}", cuts=tuple(s * cfg.n_layers // n for s in range(1, n)))
     ctx = args.ctx if args.ctx is not None else cfg.ctx
     M = args.verify  # verify rows per step (one sequence), 0 = ordinary decode
     if M:
