@@ -246,6 +246,16 @@ int decode_step_device(lps_model* m, const int32_t* tokens, const int32_t* pos, 
 /* Block until every stream of the model is idle; reports device-side errors. */
 int model_synchronize(lps_model* m);
 
+/* Test hook: the SM cycles that every bounded device-side wait of this model's
+ * kernels (a copy into a shared-memory ring, a ring slot's release) may take
+ * before the kernel gives up, records an error and returns; 0 restores the
+ * default of about two seconds. A kernel that gives up still waits, with its
+ * own fixed bound, for the copies it has issued before it ends, and the next
+ * readback or model_synchronize returns LPS_ECUDA with a message naming the
+ * kernel that failed first; the model is then unusable. Synchronizes the model
+ * first. LPS_EINVAL for cycles < 0. */
+int model_set_wait_limit(lps_model* m, long long cycles);
+
 /* Switch step overlap off (serial = 1: stage 0 of a step waits for the last
  * stage of the previous step, as LPS_FLAG_SERIAL_STEPS does at bind time) or
  * back on (serial = 0). Synchronizes the model first; results are unchanged
@@ -344,14 +354,27 @@ int model_trace_disable(lps_model* m);
  * The first call on a device looks up the array's address there. All calls
  * share the array (it keeps the last call's contents; the counters are
  * cleared by each call): calls that overlap on the GPU race, so keep them in
- * order on one stream. LPS_EINVAL for unsupported shapes or when the call
- * would need more scratch than the array holds (message from
- * attention_decode_noalloc_error()); LPS_ECUDA if a CUDA call fails. */
+ * order on one stream. LPS_EINVAL for unsupported shapes, for
+ * batch * n_kv_heads * max_ctx >= 2^31 (cache rows are addressed with 32-bit
+ * coordinates), or when the call would need more scratch than the array holds
+ * (message from attention_decode_noalloc_error()); LPS_ECUDA if a CUDA call
+ * fails. A device-side wait that gives up (a copy that never lands) is not
+ * seen by this call, which only enqueues: it sets a status word in the array,
+ * and attention_decode_noalloc_status() reports it. */
 #define LPS_NOALLOC_SCRATCH_BYTES (8u << 20)
 int attention_decode_noalloc(const float* q, const void* k_cache, const void* v_cache, float* out, int batch,
                              int n_q_heads, int n_kv_heads, int head_dim, int max_ctx, const int32_t* pos,
                              void* stream);
 const char* attention_decode_noalloc_error(void);
+
+/* Synchronize `stream` (cudaStream_t, NULL: the default stream) and read the
+ * status word that attention_decode_noalloc's kernel sets on the current
+ * device when one of its bounded waits gives up. LPS_OK: no call since the
+ * last check failed on the device. LPS_ECUDA: at least one call's `out` is
+ * invalid (message from attention_decode_noalloc_error(), naming the kernel);
+ * the word is then cleared. The word is shared by all calls on the device,
+ * like the rest of the array. Allocates nothing. */
+int attention_decode_noalloc_status(void* stream);
 
 /* The scratch bytes attention_decode_noalloc needs for these shapes on the
  * current device (the call is refused when they exceed

@@ -124,6 +124,20 @@ class _TorchMemory:
         self.free = _capi.FREE_FN(_free)
 
 
+def weights_struct(weights: dict, n_layers: int) -> "_capi.ModelWeights":
+    """The C ABI's lps_model_weights over the host arrays of ``weights`` (which
+    must stay alive while the struct is used)."""
+    layers = (_capi.LayerWeights * n_layers)()
+    for l, lw in enumerate(weights["layers"]):
+        layers[l] = _capi.LayerWeights(_ptr(lw["attn_norm"]), _matrix(lw["wq"]), _matrix(lw["wk"]),
+                                       _matrix(lw["wv"]), _matrix(lw["wo"]), _ptr(lw["ffn_norm"]),
+                                       _matrix(lw["w_gate"]), _matrix(lw["w_up"]), _matrix(lw["w_down"]))
+    w = _capi.ModelWeights(_matrix(weights["embed"]), _ptr(weights["out_norm"]), _matrix(weights["lm_head"]),
+                           layers)
+    w._layers = layers  # keep the array alive with the struct
+    return w
+
+
 class Model:
     """A model bound to one GPU over a stage plan (see ``model_bind``)."""
 
@@ -133,13 +147,7 @@ class Model:
         self.desc = _capi.ModelDesc(**desc)
         self.B, self.V = self.desc.batch, self.desc.vocab
         self._keep = weights  # host arrays must stay alive during bind only, but keep for clarity
-        layers = (_capi.LayerWeights * self.desc.n_layers)()
-        for l, lw in enumerate(weights["layers"]):
-            layers[l] = _capi.LayerWeights(_ptr(lw["attn_norm"]), _matrix(lw["wq"]), _matrix(lw["wk"]),
-                                           _matrix(lw["wv"]), _matrix(lw["wo"]), _ptr(lw["ffn_norm"]),
-                                           _matrix(lw["w_gate"]), _matrix(lw["w_up"]), _matrix(lw["w_down"]))
-        w = _capi.ModelWeights(_matrix(weights["embed"]), _ptr(weights["out_norm"]), _matrix(weights["lm_head"]),
-                               layers)
+        w = weights_struct(weights, self.desc.n_layers)
         if use_torch is None:
             try:
                 import torch
@@ -252,6 +260,10 @@ class Model:
 
     def trace_disable(self):
         _check(load().model_trace_disable(self.h))
+
+    def set_wait_limit(self, cycles: int):
+        """Test hook: the SM cycles a device-side wait may take before the kernel reports an error (0: default)."""
+        _check(load().model_set_wait_limit(self.h, int(cycles)))
 
     def set_serial_steps(self, serial: bool):
         _check(load().model_set_serial_steps(self.h, int(serial)))

@@ -33,7 +33,7 @@ EXPORTS = (
     "last_error_string", "model_stats", "model_kv_export", "model_kv_import", "model_attn_out",
     "model_time_kernel", "model_kernel_time", "model_set_serial_steps", "attention_decode_noalloc", "attention_decode_noalloc_error",
     "attention_decode_noalloc_scratch_bytes", "model_trace_enable", "model_trace_read", "model_trace_disable",
-    "stage_plan_solve", "model_stage_bytes",
+    "stage_plan_solve", "model_stage_bytes", "model_set_wait_limit", "attention_decode_noalloc_status",
 )
 
 
@@ -114,12 +114,14 @@ def load(path: str = LIB_PATH):
         "model_attn_out": (i, [vp, i, i, vp]),
         "model_time_kernel": (i, [vp, i, i]),
         "model_set_serial_steps": (i, [vp, i]),
+        "model_set_wait_limit": (i, [vp, ctypes.c_longlong]),
         "model_kernel_time": (i, [vp, i, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_uint64)]),
         "model_trace_enable": (i, [vp, i]),
         "model_trace_read": (i, [vp, ctypes.POINTER(TraceRecord), i, ctypes.POINTER(i), ctypes.POINTER(ctypes.c_uint64)]),
         "model_trace_disable": (i, [vp]),
         "attention_decode_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, i, vp, vp]),
         "attention_decode_noalloc_error": (ctypes.c_char_p, []),
+        "attention_decode_noalloc_status": (i, [vp]),
         "attention_decode_noalloc_scratch_bytes": (ctypes.c_longlong, [i, i, i, i, i]),
         "stage_plan_solve": (i, [i, i, vp, vp, vp, vp, ctypes.c_int64, vp, ctypes.POINTER(ctypes.c_int64)]),
         "model_stage_bytes": (i, [ctypes.POINTER(ModelDesc), vp, vp, ctypes.POINTER(ctypes.c_uint64),

@@ -199,13 +199,14 @@ __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const __grid_constant
 
   for (int j = 0; j < nsub; ++j) {
     const int slot = j % kRing;
-    const bool got = mbar_wait(&sm.full[slot], (j / kRing) & 1);
+    const bool got = mbar_wait(&sm.full[slot], (j / kRing) & 1, wait_cycles(p.wait_limit));
     if (__syncthreads_or(!got)) {
+      // The copies issued so far (sub-tiles j .. issued-1) land before the CTA ends.
       if (tid == 0) {
-        report_error(p.status, kErrWaitFull | (5 << 8));
-        for (int k = j + 1; k < min(nsub, j + kRing); ++k)
-          if (!mbar_wait(&sm.full[k % kRing], (k / kRing) & 1, 200000000ll)) {
-            report_error(p.status, kErrDrain);
+        report_error(p.status, kErrWaitFull | (kKidAttn << 8));
+        for (int k = j; k < issued; ++k)
+          if (!mbar_wait(&sm.full[k % kRing], (k / kRing) & 1, kDrainLimitCycles)) {
+            report_error(p.status, kErrDrain | (kKidAttn << 8));
             break;
           }
       }
@@ -304,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const __grid_constant
       }
     }
     __syncthreads();  // sub-tile `slot` fully consumed
-    if (tid == 0 && j + kRing < nsub) issue(j + kRing);
+    if (tid == 0 && j + kRing < nsub) issue(issued++);
   }
 
   // this warp's (m, l, o) per head: rows 2h (hi) and 2h+1 (lo) of o add up
@@ -400,8 +401,14 @@ __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const __grid_constant
         {
           // phases of full[0] continue from the ring's count
           const int phase = (nsub + kRing - 1) / kRing + loads++;
-          if (!mbar_wait(&sm.full[0], phase & 1)) {
-            if (tid == 0) report_error(p.status, kErrWaitFull | (6 << 8));
+          const bool ok = mbar_wait(&sm.full[0], phase & 1, wait_cycles(p.wait_limit));
+          if (__syncthreads_or(!ok)) {
+            // the staged copy lands before the CTA ends
+            if (tid == 0) {
+              report_error(p.status, kErrWaitFull | (kKidAttnCombine << 8));
+              if (!mbar_wait(&sm.full[0], phase & 1, kDrainLimitCycles))
+                report_error(p.status, kErrDrain | (kKidAttnCombine << 8));
+            }
             return;
           }
         }
@@ -457,12 +464,9 @@ template <int HD, int G>
 cudaError_t launch_hg(const AttnParams& p, int batch, int max_pos, cudaStream_t s, bool pdl) {
   auto kern = attn_kernel<HD, G>;
   const int smem = static_cast<int>(sizeof(AttnSmem<HD, G>));
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<int> smem_set[kMaxDevices];
+  cudaError_t e = set_smem_attr(kern, smem, smem_set);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((max_pos + 1 + p.chunk - 1) / p.chunk, p.nkv, batch);
   cfg.blockDim = dim3(kThreads);

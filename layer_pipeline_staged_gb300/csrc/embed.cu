@@ -14,7 +14,7 @@ __global__ void __launch_bounds__(256) embed_kernel(const __grid_constant__ Embe
   const int tok = p.tok_dev ? p.tok_dev[b] : p.tok[b];
   pdl_wait();  // the previous step may still be reading h
   if (tok < 0 || tok >= p.vocab) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) report_error(p.status, kErrBadArg);
+    if (threadIdx.x == 0 && blockIdx.x == 0) report_error(p.status, kErrBadArg | (kKidEmbed << 8));
     return;
   }
   float* h = p.h + static_cast<size_t>(b) * p.d;

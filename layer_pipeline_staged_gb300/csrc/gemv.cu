@@ -43,7 +43,6 @@ constexpr int kMaxBuf = 16;
 constexpr int kMaxRows = 4;         // rows per buffer
 constexpr int kBufTarget = 16 * 1024;
 constexpr int kReserve = 2 * kMaxBuf * 8 + kMaxWarps * 4 + 64;  // barriers + norm partials
-constexpr long long kDrainLimitCycles = 200000000ll;  // about 0.1 s
 
 template <bool INT8>
 struct Elem {
@@ -81,6 +80,11 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) gemv_kernel(const __g
   extern __shared__ __align__(1024) uint8_t smem[];
   constexpr int EB = Elem<INT8>::kBytes;
   constexpr int NP = Elem<INT8>::kPlanes;
+  // error-report ids follow the epilogues' order
+  static_assert(kEpiQkv + 1 == kKidQkv && kEpiResidual + 1 == kKidResidual && kEpiSwiglu + 1 == kKidSwiglu &&
+                    kEpiStore + 1 == kKidHead,
+                "kernel ids");
+  constexpr int kid = EPI + 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NW = p.nwarps;
   const int G = gridDim.x, cta = blockIdx.x;
@@ -117,8 +121,9 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) gemv_kernel(const __g
     const int IL = p.nbuf % kIssueLanes == 0 ? kIssueLanes : 1;
     const uint64_t pol = l2_evict_first();
     const uint8_t* src = static_cast<const uint8_t*>(p.w) + static_cast<size_t>(u0) * unit_bytes;
+    const long long limit = wait_cycles(p.wait_limit);
     int i = lane;
-    bool done = lane >= IL || i >= nbufs;
+    bool done = lane >= IL || i >= nbufs, failed = false;
     long long t0 = cycles();
     while (true) {
       bool ready = false;
@@ -133,12 +138,24 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) gemv_kernel(const __g
         i += IL;
         done = i >= nbufs;
         t0 = cycles();
-      } else if (!done && cycles() - t0 > kWaitLimitCycles) {
-        report_error(p.status, kErrWaitEmpty | ((EPI + 1) << 8));
-        done = true;
+      } else if (!done && cycles() - t0 > limit) {
+        report_error(p.status, kErrWaitEmpty | (kid << 8));
+        done = failed = true;
       }
       if (__all_sync(0xffffffffu, done)) break;
       if (!__any_sync(0xffffffffu, ready)) __nanosleep(64);  // nothing to issue yet
+    }
+    {
+      // Consumers may have left early after an error: the last buffer this
+      // lane issued into each slot lands before the CTA may end (that slot's
+      // phase cannot move past it, since nothing later was issued there). On
+      // the normal path these copies have landed or are about to.
+      (void)failed;
+      for (int j = max(lane, i - IL * (p.nbuf / IL)); j < i; j += IL)
+        if (!mbar_wait(&full[j % p.nbuf], (j / p.nbuf) & 1, kDrainLimitCycles)) {
+          report_error(p.status, kErrDrain | (kid << 8));
+          break;
+        }
     }
     return;
   }
@@ -249,16 +266,11 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) gemv_kernel(const __g
       }
       if (EPI == kEpiResidual) e0 = p.h_in[u];
     }
-    if (!mbar_wait(&full[slot], (i / p.nbuf) & 1)) {
-      // A copy never arrived: record it, let this warp drain its own later buffers, stop.
+    if (!mbar_wait(&full[slot], (i / p.nbuf) & 1, wait_cycles(p.wait_limit))) {
+      // A copy did not arrive in time: record it and stop; the producer waits
+      // for the copies it issued before the CTA ends.
       if (lane == 0) {
-        report_error(p.status, kErrWaitFull | ((EPI + 1) << 8) | (i << 12));
-        for (int j = i + NW; j < min(nbufs, i + p.nbuf); j += NW) {
-          if (!mbar_wait(&full[j % p.nbuf], (j / p.nbuf) & 1, kDrainLimitCycles)) {
-            report_error(p.status, kErrDrain);
-            break;
-          }
-        }
+        report_error(p.status, kErrWaitFull | (kid << 8) | (min(i, 0x3ffff) << 13));
       }
       return;
     }
@@ -338,17 +350,13 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) gemv_kernel(const __g
   trace_end(p.trace);
 }
 
-int g_max_smem = 0;
 
 template <bool INT8, bool NORM, int EPI, int RB>
 cudaError_t launch_rb(const GemvParams& p, const GemvPlan& plan, cudaStream_t s, bool pdl) {
   auto kern = gemv_kernel<INT8, NORM, EPI, RB>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g_max_smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<int> smem_set[kMaxDevices];
+  cudaError_t e = set_smem_attr(kern, plan.smem, smem_set);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.grid);
   cfg.blockDim = dim3((plan.nwarps + 1) * 32);
@@ -417,7 +425,6 @@ bool gemv_supported(int K, int unit_rows, bool int8, int max_smem) {
   return 2 * unit_rows * row_bytes + K * 4 + kReserve <= max_smem;
 }
 
-void gemv_set_max_smem(int bytes) { g_max_smem = bytes; }
 
 cudaError_t launch_gemv(const GemvParams& p, int epi, bool norm, bool int8, const GemvPlan& plan, cudaStream_t s,
                         bool pdl) {

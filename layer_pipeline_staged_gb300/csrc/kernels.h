@@ -7,9 +7,36 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <string>
+
 namespace lps {
 
 constexpr int kMaxBatch = 8;
+constexpr int kMaxDevices = 64;
+
+// A device-side status (two words: error kinds OR-ed, the first report whole;
+// see ptx.cuh) as a message naming the kernel that reported first.
+std::string describe_status(int kinds, int first);
+
+// The opt-in dynamic shared memory of a kernel belongs to each device's
+// context: set it on the current device unless `done` (the launcher's own
+// per-device record) shows at least `bytes` there already. Thread-safe.
+template <class Kern>
+cudaError_t set_smem_attr(Kern kern, int bytes, std::atomic<int>* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool tracked = dev >= 0 && dev < kMaxDevices;
+  if (tracked && done[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && tracked) {
+    int cur = done[dev].load(std::memory_order_relaxed);
+    while (cur < bytes && !done[dev].compare_exchange_weak(cur, bytes, std::memory_order_release)) {
+    }
+  }
+  return e;
+}
 
 // ---- weight-streaming GEMV (batch 1) --------------------------------------
 // y = W x over a row-major weight matrix whose rows are grouped into "units"
@@ -43,7 +70,8 @@ struct GemvParams {
   const float2* rope;   // (cos, sin) [hd/2] at this step's position
   int nq, nkv, hd, max_ctx, pos;
   int nwarps;           // consumer warps (set from the plan at launch)
-  int* status;
+  long long wait_limit; // cycles a buffer wait may take before it reports an error (<= 0: default)
+  int* status;          // int[2]: error kinds, first error (see ptx.cuh)
   unsigned long long* trace;  // launch trace record, or nullptr
 };
 
@@ -52,7 +80,6 @@ struct GemvPlan {
 };
 GemvPlan gemv_plan(int rows, int K, int unit_rows, bool int8, int num_sms, int max_smem);
 bool gemv_supported(int K, int unit_rows, bool int8, int max_smem);
-void gemv_set_max_smem(int bytes);
 cudaError_t launch_gemv(const GemvParams& p, int epi, bool norm, bool int8, const GemvPlan& plan,
                         cudaStream_t s, bool pdl);
 
@@ -76,6 +103,7 @@ struct SkinnyParams {
   const float2* rope;      // the whole (cos, sin) table [max_ctx][hd/2]
   int nq, nkv, hd, max_ctx;
   int pos[kMaxBatch];
+  long long wait_limit;    // cycles a stage wait may take before it reports an error (<= 0: default)
   int* status;
   unsigned long long* trace;  // launch trace record, or nullptr
 };
@@ -92,7 +120,6 @@ SkinnyPlan skinny_plan(int rows, int K, bool int8, int batch, int num_sms, int m
 // Complete a plan whose grid, units, kc, kw, pu and rc are set; false if it does not fit.
 bool skinny_plan_finish(SkinnyPlan& g, int K, bool int8, int batch, int max_smem);
 bool skinny_supported(int rows, int K, bool int8, int batch, int num_sms, int max_smem);
-void skinny_set_max_smem(int bytes);
 __host__ __device__ size_t skinny_offset(int r, int k, int kp, int kc, int units, int grid, int eb);
 cudaError_t launch_skinny(const SkinnyParams& p, int epi, bool norm, bool int8, const SkinnyPlan& plan,
                           cudaStream_t s, bool pdl);
@@ -116,6 +143,7 @@ struct AttnParams {
   float scale;                 // 1/sqrt(hd)
   int early_dependents;        // 1: let the next kernel launch once every CTA has started
                                // (pays when it is the batch-1 GEMV), 0: once every CTA ends
+  long long wait_limit;        // cycles a sub-tile wait may take before it reports an error (<= 0: default)
   int* status;
   unsigned long long* trace;  // launch trace record, or nullptr
 };

@@ -19,6 +19,11 @@
 // (on the caller's stream). Two calls whose work overlaps on the GPU -- on
 // different streams, or on different host threads -- race on the array and
 // give wrong results; order them on one stream.
+//
+// The array's first 256 bytes hold a status (two ints) that the kernel sets
+// when one of its bounded waits gives up, in which case that call's output is
+// invalid. The status is sticky across calls: attention_decode_noalloc_status
+// reads it (after synchronizing the caller's stream) and clears it.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -39,13 +44,12 @@ bool attn_supported(int hd, int group);
 namespace {
 
 constexpr size_t kScratchBytes = LPS_NOALLOC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-int g_num_sms[kMaxDevices] = {};
+void* g_scratch_addr[lps::kMaxDevices] = {};
+int g_num_sms[lps::kMaxDevices] = {};
 
 thread_local std::string g_err;
 
@@ -53,6 +57,11 @@ int fail(int code, const std::string& why) {
   g_err = "attention_decode_noalloc: " + why;
   return code;
 }
+
+// Scratch layout: the status (two ints) in a 256-byte block, the chunk
+// counters [B][nkv] (rounded up to 256 bytes), then the partials
+// [B][nq][nchunks][hd + 4] floats.
+constexpr size_t kStatusBytes = 256;
 
 // The array's device address on device `dev` (which must be current).
 cudaError_t scratch_on(int dev, void** addr, int* num_sms) {
@@ -99,10 +108,10 @@ bool encode_cache(CUtensorMap* map, const void* base, int hd, unsigned long long
 extern "C" const char* attention_decode_noalloc_error(void) { return g_err.c_str(); }
 
 namespace {
-// Scratch of one call: the counters (rounded up to 256 bytes) and the partials.
+// Scratch of one call: the status block and the counters (each rounded up to 256 bytes), then the partials.
 void scratch_need(int batch, int n_q_heads, int n_kv_heads, int head_dim, int nchunks, size_t* counter_bytes,
                   size_t* part_bytes) {
-  *counter_bytes = (static_cast<size_t>(batch) * n_kv_heads * sizeof(int) + 255) / 256 * 256;
+  *counter_bytes = kStatusBytes + (static_cast<size_t>(batch) * n_kv_heads * sizeof(int) + 255) / 256 * 256;
   *part_bytes = static_cast<size_t>(batch) * n_q_heads * nchunks * (head_dim + 4) * sizeof(float);
 }
 }  // namespace
@@ -141,16 +150,17 @@ extern "C" int attention_decode_noalloc(const float* q, const void* k_cache, con
   }
   if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15)
     return fail(LPS_EINVAL, "caches must be 16-byte aligned");
+  // the kernel addresses cache rows with 32-bit TMA coordinates
+  if (static_cast<long long>(batch) * n_kv_heads * max_ctx > 0x7fffffffll)
+    return fail(LPS_EINVAL, "batch * n_kv_heads * max_ctx must stay below 2^31 cache rows");
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return fail(LPS_ECUDA, "no usable current device");
+  if (e != cudaSuccess || dev < 0 || dev >= lps::kMaxDevices) return fail(LPS_ECUDA, "no usable current device");
   void* base = nullptr;
   int num_sms = 0;
   e = scratch_on(dev, &base, &num_sms);
   if (e != cudaSuccess) return fail(LPS_ECUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
 
-  // scratch layout: counters [B][nkv] int (256-byte block), then partials
-  // [B][nq][nchunks][hd + 4] floats
   const int chunk = attn_chunk(head_dim, n_kv_heads, batch, max_pos, num_sms);
   const int nchunks = (max_pos + 1 + chunk - 1) / chunk;
   size_t counter_bytes = 0, part_bytes = 0;
@@ -160,7 +170,7 @@ extern "C" int attention_decode_noalloc(const float* q, const void* k_cache, con
                                 std::to_string(kScratchBytes) + " this entry point holds; use fewer sequences or "
                                 "positions, or the regular decode path");
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  e = cudaMemsetAsync(base, 0, counter_bytes, s);
+  e = cudaMemsetAsync(static_cast<unsigned char*>(base) + kStatusBytes, 0, counter_bytes - kStatusBytes, s);
   if (e != cudaSuccess) return fail(LPS_ECUDA, std::string("clearing the counters: ") + cudaGetErrorString(e));
 
   AttnParams p{};
@@ -172,7 +182,7 @@ extern "C" int attention_decode_noalloc(const float* q, const void* k_cache, con
   p.kc = static_cast<const __nv_bfloat16*>(k_cache);
   p.vc = static_cast<const __nv_bfloat16*>(v_cache);
   p.out = out;
-  p.counter = static_cast<int*>(base);
+  p.counter = reinterpret_cast<int*>(static_cast<unsigned char*>(base) + kStatusBytes);
   p.part = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + counter_bytes);
   p.nq = n_q_heads;
   p.nkv = n_kv_heads;
@@ -182,8 +192,27 @@ extern "C" int attention_decode_noalloc(const float* q, const void* k_cache, con
   p.chunk = chunk;
   for (int b = 0; b < batch; ++b) p.pos[b] = pos[b];
   p.scale = 1.0f / std::sqrt(static_cast<float>(head_dim));
-  p.status = nullptr;
+  p.status = static_cast<int*>(base);  // sticky until attention_decode_noalloc_status reads it
   e = launch_attention(p, batch, max_pos, s, false);
   if (e != cudaSuccess) return fail(LPS_ECUDA, std::string("launch: ") + cudaGetErrorString(e));
   return LPS_OK;
+}
+
+extern "C" int attention_decode_noalloc_status(void* stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= lps::kMaxDevices) return fail(LPS_ECUDA, "no usable current device");
+  void* base = nullptr;
+  int num_sms = 0;
+  e = scratch_on(dev, &base, &num_sms);
+  if (e != cudaSuccess) return fail(LPS_ECUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+  e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(LPS_ECUDA, std::string("stream: ") + cudaGetErrorString(e));
+  int st[2] = {0, 0};
+  e = cudaMemcpy(st, base, sizeof st, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(LPS_ECUDA, std::string("reading the status: ") + cudaGetErrorString(e));
+  if (st[0] == 0 && st[1] == 0) return LPS_OK;
+  e = cudaMemset(base, 0, sizeof st);
+  if (e != cudaSuccess) return fail(LPS_ECUDA, std::string("clearing the status: ") + cudaGetErrorString(e));
+  return fail(LPS_ECUDA, "an earlier call's output is invalid: " + lps::describe_status(st[0], st[1]));
 }

@@ -8,19 +8,45 @@
 
 namespace lps {
 
-// Device-side error bits, OR-ed into the model's status word.
+// Device-side error reports. A status is two ints: word 0 collects the kind
+// bits below (OR-ed), word 1 keeps the first report whole (kind bits, the
+// kernel id at bits 8..11 and a detail above), so the host can name the
+// kernel that failed first.
 enum : int {
   kErrWaitFull = 1,    // a consumer gave up waiting for a bulk copy
   kErrWaitEmpty = 2,   // a producer gave up waiting for a buffer to be released
   kErrDrain = 4,       // draining in-flight copies after an error also timed out
   kErrBadArg = 8,      // a kernel saw an argument outside its supported range
+  kErrBarrier = 16,    // a grid-wide barrier wait gave up
+};
+// Kernel ids of the reports (bits 8..11); bit 12 marks the batch > 1 GEMM.
+enum : int {
+  kKidQkv = 1,         // RMSNorm + QKV + RoPE + KV append
+  kKidResidual = 2,    // o-proj or down projection + residual
+  kKidSwiglu = 3,      // RMSNorm + gate/up + SwiGLU
+  kKidHead = 4,        // final RMSNorm + LM head
+  kKidAttn = 5,        // split-K attention
+  kKidAttnCombine = 6, // split-K attention, the last CTA's merge
+  kKidEmbed = 7,       // embedding row
+  kKidStage = 8,       // the persistent stage kernel
+  kKidSkinnyBit = 1 << 12,
 };
 
 // Every mbarrier wait gives up after this many SM cycles (about two seconds at
-// the maximum clock). The per-SM cycle counter is used because it is monotonic
-// on the SM that spins; a global timer read can step backwards between SMs'
-// updates, and an unsigned difference of two such reads would wrap.
+// the maximum clock) unless a kernel's parameters set a shorter limit (a test
+// hook). The per-SM cycle counter is used because it is monotonic on the SM
+// that spins; a global timer read can step backwards between SMs' updates, and
+// an unsigned difference of two such reads would wrap.
 constexpr long long kWaitLimitCycles = 4000000000ll;
+// Waiting for the copies a thread issued itself to land before its CTA ends
+// (after an error) keeps this bound, whatever the parameters say: a copy must
+// never land in the shared memory of a CTA that has ended.
+constexpr long long kDrainLimitCycles = 200000000ll;  // about 0.1 s
+
+// The wait limit a kernel uses: the parameter when positive, else the default.
+__host__ __device__ __forceinline__ long long wait_cycles(long long param) {
+  return param > 0 ? param : kWaitLimitCycles;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -140,8 +166,12 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-__device__ __forceinline__ void report_error(int* status, int bits) {
-  if (status) atomicOr(status, bits);
+// Record an error: `code` = kind bits | kernel id << 8 | detail << 13.
+__device__ __forceinline__ void report_error(int* status, int code) {
+  if (status) {
+    atomicOr(status, code & 0xff);
+    atomicCAS(status + 1, 0, code);
+  }
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -59,6 +59,33 @@ int cuda_fail(const char* fn, const char* what, cudaError_t e) {
 namespace lps {
 // The thread's last error, for host code in other files (the stage solver).
 int host_fail(int code, const char* fn, const std::string& why) { return fail(code, fn, why); }
+
+std::string describe_status(int kinds, int first) {
+  static const char* const kKernels[] = {"unknown kernel",
+                                         "RMSNorm + QKV + RoPE + KV append",
+                                         "o-proj / down projection + residual",
+                                         "RMSNorm + gate/up + SwiGLU",
+                                         "final RMSNorm + LM head",
+                                         "split-K attention",
+                                         "split-K attention (merge of the chunks)",
+                                         "embedding",
+                                         "persistent stage kernel"};
+  const int kid = (first >> 8) & 0xf;
+  std::string what;
+  const int k = first & 0xff ? first & 0xff : kinds;
+  if (k & 1) what += "a copy wait timed out; ";
+  if (k & 2) what += "a buffer-release wait timed out; ";
+  if (k & 4) what += "draining in-flight copies timed out; ";
+  if (k & 8) what += "a kernel argument was out of range; ";
+  if (k & 16) what += "a grid-wide barrier wait timed out; ";
+  if (what.empty()) what = "unknown error; ";
+  std::string name = kKernels[kid < 9 ? kid : 0];
+  if (first & 0x1000) name += " (batch > 1 tensor-core GEMM)";
+  char buf[96];
+  std::snprintf(buf, sizeof buf, "(status 0x%x, first report 0x%x, detail %d)", kinds, first,
+                static_cast<int>(static_cast<unsigned>(first) >> 13));
+  return "device-side error in " + name + ": " + what + buf;
+}
 }  // namespace lps
 
 // ---------------------------------------------------------------------------
@@ -229,6 +256,7 @@ struct lps_model {
   uint64_t step_count = 0;
   lps_stats stats{};
   bool failed = false;
+  long long wait_limit = 0;  // device-side wait limit in cycles (0: the kernels' default)
   int attn_max_chunks = 0;
   KTimer timers[7];
   // launch trace: device records [cap][2] (zeroed), host metadata per record
@@ -536,6 +564,9 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
                                   "at most 64 16-row units (1024 rows) per SM");
   }
   if (!(d.rms_eps > 0.f) || !(d.rope_theta > 0.f)) return fail(LPS_EINVAL, FN, "rms_eps and rope_theta must be > 0");
+  // the attention addresses a layer's cache rows with 32-bit TMA coordinates
+  if (static_cast<long long>(d.batch) * d.n_kv_heads * d.max_ctx > 0x7fffffffll)
+    return fail(LPS_EINVAL, FN, "batch * n_kv_heads * max_ctx must stay below 2^31 cache rows per layer");
   if (!w->layers || !w->out_norm || !w->embed.w || !w->lm_head.w) return fail(LPS_EINVAL, FN, "missing weights");
 
   lps_model* m = new lps_model();
@@ -579,8 +610,6 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
   if (e != cudaSuccess) return bail(LPS_ECUDA, std::string("cudaSetDevice: ") + cudaGetErrorString(e));
   if (cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) != cudaSuccess)
     return bail(LPS_ECUDA, "cudaDeviceGetAttribute failed");
-  gemv_set_max_smem(max_smem);
-  skinny_set_max_smem(max_smem);
 
   const int N = m->N, B = d.batch, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads, E = d.n_embd;
   const int half = hd / 2;
@@ -621,10 +650,10 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
                                                             static_cast<float>(std::sin(ang)));
     }
 
-  m->status_dev = static_cast<int*>(dev_alloc(m, sizeof(int)));
-  m->status_host = static_cast<int*>(host_alloc(m, sizeof(int)));
+  m->status_dev = static_cast<int*>(dev_alloc(m, 2 * sizeof(int)));
+  m->status_host = static_cast<int*>(host_alloc(m, 2 * sizeof(int)));
   if (!m->status_dev || !m->status_host) return bail(LPS_ENOMEM, "status word allocation failed");
-  if (cudaMemset(m->status_dev, 0, sizeof(int)) != cudaSuccess) return bail(LPS_ECUDA, "cudaMemset failed");
+  if (cudaMemset(m->status_dev, 0, 2 * sizeof(int)) != cudaSuccess) return bail(LPS_ECUDA, "cudaMemset failed");
 
   const int seqs = m->verify ? 1 : B;  // sequences with a cache of their own
   const size_t kv_elems = static_cast<size_t>(seqs) * nkv * d.max_ctx * hd;
@@ -797,7 +826,7 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
   for (auto& p : m->pend) {
     p.logits_dev = static_cast<float*>(dev_alloc(m, logits_bytes));
     p.host = static_cast<float*>(host_alloc(m, logits_bytes));
-    p.status_host = static_cast<int*>(host_alloc(m, sizeof(int)));
+    p.status_host = static_cast<int*>(host_alloc(m, 2 * sizeof(int)));
     if (!p.logits_dev || !p.host || !p.status_host) return bail(LPS_ENOMEM, "pending slot allocation failed");
     if (cudaEventCreateWithFlags(&p.ev_done, cudaEventDisableTiming) != cudaSuccess)
       return bail(LPS_ECUDA, "cudaEventCreate failed");
@@ -861,6 +890,7 @@ SkinnyParams skinny_params(const lps_model* m, const void* w, const float* wscal
   p.kv_stride = m->verify ? 0 : static_cast<size_t>(m->d.n_kv_heads) * m->d.max_ctx * m->d.head_dim;
   for (int b = 0; b < m->d.batch; ++b) p.pos[b] = pos[b];
   p.status = m->status_dev;
+  p.wait_limit = m->wait_limit;
   return p;
 }
 
@@ -966,6 +996,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
         p.max_ctx = d.max_ctx;
         p.pos = pos[b];
         p.status = m->status_dev;
+        p.wait_limit = m->wait_limit;
         LAUNCH(LPS_KERNEL_QKV, cs, p, launch_gemv(p, kEpiQkv, true, m->int8, S.plan_qkv, cs, pdl));
       }
       // split-K attention over [0, pos]
@@ -989,6 +1020,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
         ap.scale = 1.0f / std::sqrt(static_cast<float>(hd));
         ap.early_dependents = m->skinny ? 0 : 1;  // the GEMV o-proj follows
         ap.status = m->status_dev;
+        ap.wait_limit = m->wait_limit;
         if (!m->verify) {
           LAUNCH(LPS_KERNEL_ATTN, cs, ap, launch_attention(ap, B, max_pos, cs, pdl));
         } else {
@@ -1029,6 +1061,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
         p.h_in = hin + static_cast<size_t>(b) * E;
         p.h_out = S.h + static_cast<size_t>(b) * E;
         p.status = m->status_dev;
+        p.wait_limit = m->wait_limit;
         LAUNCH(LPS_KERNEL_OPROJ, cs, p, launch_gemv(p, kEpiResidual, false, m->int8, S.plan_o, cs, pdl));
       }
       if (first && s > 0 && !m->single) CK(cudaEventRecord(m->bd[s - 1].ev_rx[par], cs), "record ev_rx");
@@ -1056,6 +1089,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
         p.eps = d.rms_eps;
         p.out = S.a + static_cast<size_t>(b) * d.ffn;
         p.status = m->status_dev;
+        p.wait_limit = m->wait_limit;
         LAUNCH(LPS_KERNEL_GATEUP, cs, p, launch_gemv(p, kEpiSwiglu, true, m->int8, S.plan_gu, cs, pdl));
       }
       // down + residual (the last layer of an earlier stage writes the boundary slot)
@@ -1082,6 +1116,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
         p.h_in = S.h + static_cast<size_t>(b) * E;
         p.h_out = h_out + static_cast<size_t>(b) * E;
         p.status = m->status_dev;
+        p.wait_limit = m->wait_limit;
         LAUNCH(LPS_KERNEL_DOWN, cs, p, launch_gemv(p, kEpiResidual, false, m->int8, S.plan_d, cs, pdl));
       }
     }
@@ -1125,6 +1160,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
       p.eps = d.rms_eps;
       p.out = logits_dev + static_cast<size_t>(b) * d.vocab;
       p.status = m->status_dev;
+      p.wait_limit = m->wait_limit;
       LAUNCH(LPS_KERNEL_HEAD, cs, p, launch_gemv(p, kEpiStore, true, m->int8, S.plan_head, cs, pdl));
     }
     if (N > 1 && !m->single && !m->overlap) CK(cudaEventRecord(m->ev_step, cs), "record step event");
@@ -1140,13 +1176,10 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
   return LPS_OK;
 }
 
-int read_status(lps_model* m, int status, const char* FN) {
-  if (status != 0) {
+int read_status(lps_model* m, const int* status, const char* FN) {
+  if (status[0] != 0 || status[1] != 0) {
     m->failed = true;
-    char buf[128];
-    std::snprintf(buf, sizeof buf, "device-side error 0x%x (1: copy wait timed out, 2: buffer wait timed out, "
-                                   "4: drain timed out, 8: bad kernel argument)", status);
-    return fail(LPS_ECUDA, FN, buf);
+    return fail(LPS_ECUDA, FN, lps::describe_status(status[0], status[1]));
   }
   return LPS_OK;
 }
@@ -1164,14 +1197,14 @@ extern "C" int decode_step(lps_model* m, const int32_t* tokens, const int32_t* p
   const cudaStream_t last = m->stream(m->N - 1);
   const size_t bytes = sizeof(float) * m->d.batch * static_cast<size_t>(m->d.vocab);
   CK(cudaMemcpyAsync(m->eager_host, m->eager_logits_dev, bytes, cudaMemcpyDeviceToHost, last), "logits copy");
-  CK(cudaMemcpyAsync(m->status_host, m->status_dev, sizeof(int), cudaMemcpyDeviceToHost, last), "status copy");
+  CK(cudaMemcpyAsync(m->status_host, m->status_dev, 2 * sizeof(int), cudaMemcpyDeviceToHost, last), "status copy");
   // the last stage's wait chain orders every earlier stage, so this drains the step
   cudaError_t e = cudaStreamSynchronize(last);
   if (e != cudaSuccess) {
     m->failed = true;
     return cuda_fail(FN, "step", e);
   }
-  rc = read_status(m, *m->status_host, FN);
+  rc = read_status(m, m->status_host, FN);
   if (rc) return rc;
   std::memcpy(logits, m->eager_host, bytes);
   return LPS_OK;
@@ -1228,7 +1261,7 @@ extern "C" int pending_wait(lps_pending* p, float* logits, int timeout_ms) {
     // the dedicated readback stream waits the completion event, copies, syncs
     CK(cudaStreamWaitEvent(m->rb, P.ev_done, 0), "readback wait");
     CK(cudaMemcpyAsync(P.host, P.logits_dev, bytes, cudaMemcpyDeviceToHost, m->rb), "logits copy");
-    CK(cudaMemcpyAsync(P.status_host, m->status_dev, sizeof(int), cudaMemcpyDeviceToHost, m->rb), "status copy");
+    CK(cudaMemcpyAsync(P.status_host, m->status_dev, 2 * sizeof(int), cudaMemcpyDeviceToHost, m->rb), "status copy");
     const cudaError_t e = cudaStreamSynchronize(m->rb);
     if (e != cudaSuccess) {
       m->failed = true;
@@ -1237,7 +1270,7 @@ extern "C" int pending_wait(lps_pending* p, float* logits, int timeout_ms) {
     P.drained = true;
     ++m->stats.pending_drains;
   }
-  const int rc = read_status(m, *P.status_host, FN);
+  const int rc = read_status(m, P.status_host, FN);
   if (rc) return rc;
   std::memcpy(logits, P.host, bytes);
   return LPS_OK;
@@ -1270,8 +1303,8 @@ extern "C" int model_synchronize(lps_model* m) {
     }
   }
   CK(cudaStreamSynchronize(m->rb), "readback stream");
-  CK(cudaMemcpy(m->status_host, m->status_dev, sizeof(int), cudaMemcpyDeviceToHost), "status copy");
-  return read_status(m, *m->status_host, FN);
+  CK(cudaMemcpy(m->status_host, m->status_dev, 2 * sizeof(int), cudaMemcpyDeviceToHost), "status copy");
+  return read_status(m, m->status_host, FN);
 }
 
 extern "C" int model_stream(const lps_model* m, int s, void** stream) {
@@ -1351,6 +1384,15 @@ extern "C" int model_attn_out(const lps_model* m, int layer, int b, float* host)
   CK(cudaSetDevice(m->device), "cudaSetDevice");
   CK(cudaStreamSynchronize(m->stream(s)), "stage stream");
   CK(cudaMemcpy(host, L.o_keep + b * qw, qw * sizeof(float), cudaMemcpyDeviceToHost), "copy");
+  return LPS_OK;
+}
+
+extern "C" int model_set_wait_limit(lps_model* m, long long cycles) {
+  static const char* FN = "model_set_wait_limit";
+  if (!m || cycles < 0) return fail(LPS_EINVAL, FN, "model and cycles >= 0 are required");
+  const int rc = model_synchronize(m);
+  if (rc) return rc;
+  m->wait_limit = cycles;
   return LPS_OK;
 }
 

@@ -45,7 +45,6 @@ constexpr int kMaxPu = 4;               // units per pass
 constexpr int kParts = 3;               // n-tiles: hi, mid and lo parts; column b = sequence b
 constexpr int kCols = 8 * kParts;       // B columns
 constexpr int kBarAll = 1;              // named barrier of the consumer warps
-constexpr long long kDrainCycles = 200000000ll;
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -200,8 +199,8 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, 1) skinny_kernel(const __gr
         }
         done = s >= S;
         t0 = cycles();
-      } else if (!done && cycles() - t0 > kWaitLimitCycles) {
-        report_error(p.status, kErrWaitEmpty | ((EPI + 1) << 8) | (1 << 11));
+      } else if (!done && cycles() - t0 > wait_cycles(p.wait_limit)) {
+        report_error(p.status, kErrWaitEmpty | ((EPI + 1) << 8) | kKidSkinnyBit);
         done = failed = true;
       }
       if (__all_sync(0xffffffffu, done)) break;
@@ -210,8 +209,8 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, 1) skinny_kernel(const __gr
     // the last stages issued land in this CTA's shared memory before it may
     // end, also when the consumers leave early (bounded)
     for (int t = max(0, s - RC); t < s; ++t)
-      if (!mbar_wait(&full[t % RC], (t / RC) & 1, failed ? kDrainCycles : kWaitLimitCycles)) {
-        report_error(p.status, kErrDrain | ((EPI + 1) << 8) | (1 << 11));
+      if (!mbar_wait(&full[t % RC], (t / RC) & 1, failed ? kDrainLimitCycles : kWaitLimitCycles)) {
+        report_error(p.status, kErrDrain | ((EPI + 1) << 8) | kKidSkinnyBit);
         break;
       }
     return;
@@ -342,9 +341,9 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, 1) skinny_kernel(const __gr
       else
         cp_async_wait_all();
       __syncwarp();
-      if (!bad && !mbar_wait_sleep(&full[slot], phase)) {
+      if (!bad && !mbar_wait_sleep(&full[slot], phase, wait_cycles(p.wait_limit))) {
         bad = true;
-        if (lane == 0) report_error(p.status, kErrWaitFull | ((EPI + 1) << 8) | (1 << 11));
+        if (lane == 0) report_error(p.status, kErrWaitFull | ((EPI + 1) << 8) | kKidSkinnyBit);
       }
       if (!bad) {
         const float* xs = xslot0 + (s & 1) * xslot_floats;
@@ -466,17 +465,13 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, 1) skinny_kernel(const __gr
   trace_end(p.trace);
 }
 
-int g_max_smem = 0;
 
 template <bool INT8, bool NORM, int EPI, int UPW, int KCB>
 cudaError_t launch_t(const SkinnyParams& p, const SkinnyPlan& plan, cudaStream_t s, bool pdl) {
   auto kern = skinny_kernel<INT8, NORM, EPI, UPW, KCB>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g_max_smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<int> smem_set[kMaxDevices];
+  cudaError_t e = set_smem_attr(kern, plan.smem, smem_set);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.grid);
   cfg.blockDim = dim3((kWarps + 1) * 32);
@@ -511,7 +506,6 @@ cudaError_t launch_e(const SkinnyParams& p, const SkinnyPlan& plan, cudaStream_t
 
 }  // namespace
 
-void skinny_set_max_smem(int bytes) { g_max_smem = bytes; }
 
 // Fill the derived fields of a plan whose grid, units, kc, pu and rc are set;
 // false if it does not fit.

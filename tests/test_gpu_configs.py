@@ -61,19 +61,37 @@ def test_padded_dummy_heads_zero_and_match_unpadded(padded):
     assert mp.stats()["fence"] == (0, 6, 15, 24)
 
 
+def _bitwise_arms(cfg, w, m, m1, toks, pos0, got):
+    """The workload's stage plan read back deferred (``got``) equals the
+    1-stage plan read back eagerly, and the workload's plan read back eagerly
+    (rewinding to pos0), bit for bit (memra_engine::pp, "M2 increment 3": the
+    pipelined replay is bit-identical per step; ninfer pipeline-stages.md,
+    "Verification": the split output equals one device byte for byte)."""
+    one = np.stack([m1.decode_step(toks[t], pos0 + t) for t in range(len(toks))])
+    assert np.array_equal(one, got), f"{cfg.name}: 1-stage differs from {cfg.fence}"
+    eager = np.stack([m.decode_step(toks[t], pos0 + t) for t in range(len(toks))])
+    assert np.array_equal(eager, got), f"{cfg.name}: eager differs from deferred"
+
+
 def test_padded_full_context_transplant(padded):
+    """Zero-padded heads, batch 4 on the tensor-core GEMM, 3 stages (cuts 6, 15),
+    context 4096: the oracle on two steps, and bit-identity with one stage and
+    with eager readback on four."""
     cfg, wp, _ = padded
     P = cfg.ctx
-    max_ctx = P + 4
+    T = 4
+    max_ctx = P + T
     m = bind(cfg, wp, max_ctx=max_ctx)
+    m1 = bind(cfg, wp, max_ctx=max_ctx, fence=(0, cfg.n_layers))
     orc = oracle.Oracle(cfg, wp, max_ctx=max_ctx)
     for (l, b), (k, v) in iter_random_kv(cfg, 41, cfg.n_layers, max_ctx, P):
-        m.kv_import(l, b, k, v, P)
-        orc.kv_import(l, b, k, v, P)
-    toks = synth.make_tokens(cfg, 2, seed=cfg.seed_t + 3)
+        for x in (m, m1, orc):
+            x.kv_import(l, b, k, v, P)
+    toks = synth.make_tokens(cfg, T, seed=cfg.seed_t + 3)
     got = _deferred_steps(m, toks, P)
     for t in range(2):
         assert_close(got[t], orc.step(toks[t], P + t), cfg, f"step {t}")
+    _bitwise_arms(cfg, wp, m, m1, toks, P, got)
 
 
 def test_1b_whole_sequence():
@@ -95,19 +113,25 @@ def test_1b_whole_sequence():
 
 @pytest.mark.parametrize("name", ["8b", "8b_q8", "8b_q8_b8"])
 def test_full_context_transplant(name):
+    """The full contexts (8B bf16 at 8192 with cuts 8/16/24; 8B int8 at 32768,
+    batch 1 and 8, cut 16): the oracle on two steps from an imported cache, and
+    bit-identity with one stage and with eager readback on four steps."""
     cfg = synth.CONFIGS[name]
     P = cfg.ctx
-    max_ctx = P + 2
+    T = 4
+    max_ctx = P + T
     w = synth.make_weights(cfg)
     m = bind(cfg, w, max_ctx=max_ctx, pending_depth=4)
+    m1 = bind(cfg, w, max_ctx=max_ctx, fence=(0, cfg.n_layers))
     orc = oracle.Oracle(cfg, w, max_ctx=max_ctx)
     for (l, b), (k, v) in iter_random_kv(cfg, 43, cfg.n_layers, max_ctx, P):
-        m.kv_import(l, b, k, v, P)
-        orc.kv_import(l, b, k, v, P)
-    toks = synth.make_tokens(cfg, 2, seed=cfg.seed_t + 5)
+        for x in (m, m1, orc):
+            x.kv_import(l, b, k, v, P)
+    toks = synth.make_tokens(cfg, T, seed=cfg.seed_t + 5)
     got = _deferred_steps(m, toks, P)
     for t in range(2):
         assert_close(got[t], orc.step(toks[t], P + t), cfg, f"{name} step {t}")
+    _bitwise_arms(cfg, w, m, m1, toks, P, got)
     # the rows this step wrote: the GPU's and the oracle's agree within one bf16 rounding
     for l in (0, cfg.n_layers - 1):
         kg, vg = m.kv_export(l, 0)
@@ -118,3 +142,25 @@ def test_full_context_transplant(name):
             scale = np.max(np.abs(b), axis=2, keepdims=True)
             assert np.all(np.abs(a - b) <= np.abs(b) * 2 ** -7 + 1e-4 * scale)
             assert np.array_equal(g_[:, :P], o_[:, :P])
+
+
+def test_8b_reduced_context_whole_sequence():
+    """The 8B shape with all 32 layers over a reduced context: 256 teacher-forced
+    positions and 16 decode steps from position 0, every cache row written by
+    the kernels, the 4-stage deferred run against the oracle at every position
+    and bit-identical to the 1-stage eager run."""
+    cfg = synth.CONFIGS["8b"]
+    T = 256 + 16
+    w = synth.make_weights(cfg)
+    toks = synth.make_tokens(cfg, T)
+    m = bind(cfg, w, max_ctx=T, pending_depth=4)
+    got = _deferred_steps(m, toks, 0)
+    m.close()
+    orc = oracle.Oracle(cfg, w, max_ctx=T)
+    worst = 0.0
+    for t in range(T):
+        worst = max(worst, assert_close(got[t], orc.step(toks[t], t), cfg, f"position {t}"))
+    orc.close()
+    m1 = bind(cfg, w, max_ctx=T, fence=(0, cfg.n_layers))
+    for t in range(T):
+        assert np.array_equal(m1.decode_step(toks[t], t), got[t]), f"1-stage differs at position {t}"

@@ -1,12 +1,15 @@
-"""attention_decode_noalloc against the regular decode step's attention.
+"""attention_decode_noalloc against the oracle's attention, head by head.
 
 The entry point exists for callers that may not allocate device memory once
 they run (a latency-bound serving loop, a program with a fixed memory pool):
-its scratch is a static device array inside the library. This test checks,
-through the C ABI, that two calls in a row give the same attention output as
-the decode step of a bound model (read with model_attn_out), within the
-tolerance the other GPU tests use. It sits in a file of its own, collected
-last, and needs nothing from the other test files' state.
+its scratch is a static device array inside the library. These tests call it
+through the C ABI on seeded q and caches, with a different position for every
+sequence (so the sequences have different chunk counts in one launch), at head
+dim 64 with one q head per kv head and at head dim 128 with eight; every
+(sequence, q head) output must match the oracle's attention of that head
+within the tolerance the other GPU tests use, and two calls in a row must give
+the same bits. The status query must then report no device-side failure. The
+file is collected last and needs nothing from the other test files' state.
 """
 import ctypes
 
@@ -14,62 +17,51 @@ import numpy as np
 import pytest
 
 import layer_pipeline_staged_gb300 as lps
+import oracle
 import synth
 from layer_pipeline_staged_gb300 import _capi
-from workloads import TOL_BF16, bind, random_kv, rel_err
+from workloads import TOL_BF16
 
 pytestmark = pytest.mark.gpu
 
-CFG = synth.ModelConfig("noalloc", 93, 2, 512, 32, 8, 128, 512, 1000, "bf16", 2, 0, 0, (1,))
 
-
-def _q_layer0(w, tok, pos):
-    """q of layer 0 for one token at `pos`: RMSNorm of the embedding row, W_q,
-    then RoPE (rotate-half pairs, angle pos * 10000^(-2i/hd))."""
-    h = synth.bf16_to_f32(w["embed"][tok]).astype(np.float64)
-    xn = h / np.sqrt(np.mean(h * h) + CFG.rms_eps) * w["layers"][0]["attn_norm"].astype(np.float64)
-    q = (synth.bf16_to_f32(w["layers"][0]["wq"]).astype(np.float64) @ xn).reshape(CFG.q_heads, CFG.head_dim)
-    half = CFG.head_dim // 2
-    ang = pos * CFG.rope_theta ** (-2.0 * np.arange(half) / CFG.head_dim)
-    a, b = q[:, :half].copy(), q[:, half:].copy()
-    q[:, :half] = a * np.cos(ang) - b * np.sin(ang)
-    q[:, half:] = a * np.sin(ang) + b * np.cos(ang)
-    return q.reshape(-1).astype(np.float32)
-
-
-def test_noalloc_attention_matches_decode_step():
+@pytest.mark.parametrize("hd,group,nkv", [(64, 1, 6), (128, 8, 2)])
+def test_noalloc_attention_matches_oracle(hd, group, nkv):
     import torch
 
-    P = 3000  # cached rows before the step: several chunks per (sequence, kv head)
-    max_ctx = P + 1
-    w = synth.make_weights(CFG)
-    m = bind(CFG, w, max_ctx=max_ctx, flags=lps.LPS_FLAG_KEEP_ATTN_OUT)
-    for (l, b), (k, v) in random_kv(CFG, 31, CFG.n_layers, max_ctx, P).items():
-        m.kv_import(l, b, k, v, P)
-    toks = synth.make_tokens(CFG, 1, seed=91)[0]
-    m.decode_step(toks, P)
-    ref = np.stack([m.attn_out(0, b).reshape(-1) for b in range(CFG.batch)])
+    B, nq = 3, nkv * group
+    pos = np.array([2999, 701, 0], np.int32)  # several chunks, a few, and a single row
+    max_ctx = 3001
+    seed = 95
+    # caches: uniform bf16 in [-1, 1); q: N(0, 3) so the scores spread over a few units
+    k = synth.uniform_bf16(seed, 0, (B, nkv, max_ctx, hd))
+    v = synth.uniform_bf16(seed, 1, (B, nkv, max_ctx, hd))
+    q = synth.normal_f32(seed, 2, (B, nq * hd), stddev=3.0)
+    ref = np.empty((B, nq, hd), np.float64)
+    for b in range(B):
+        for h in range(nq):
+            g = h // group
+            ref[b, h] = oracle.attend_head(q[b, h * hd:(h + 1) * hd].astype(np.float64), k[b, g], v[b, g], int(pos[b]))
 
-    # inputs of the regular step's layer-0 attention: its cache (row P included) and q
-    kv = [m.kv_export(0, b) for b in range(CFG.batch)]
-    k_dev = torch.tensor(np.stack([x[0] for x in kv]).view(np.int16), device="cuda")
-    v_dev = torch.tensor(np.stack([x[1] for x in kv]).view(np.int16), device="cuda")
-    q_dev = torch.tensor(np.stack([_q_layer0(w, toks[b], P) for b in range(CFG.batch)]), device="cuda")
-    out_dev = torch.full((CFG.batch, CFG.q_heads * CFG.head_dim), float("nan"), device="cuda")
-    pos = (ctypes.c_int32 * CFG.batch)(*([P] * CFG.batch))
+    k_dev = torch.tensor(k.view(np.int16), device="cuda")
+    v_dev = torch.tensor(v.view(np.int16), device="cuda")
+    q_dev = torch.tensor(q, device="cuda")
+    out_dev = torch.full((B, nq * hd), float("nan"), device="cuda")
+    cpos = (ctypes.c_int32 * B)(*pos.tolist())
     L = _capi.load()
     stream = torch.cuda.current_stream().cuda_stream
 
     results = []
     for call in range(2):
-        rc = L.attention_decode_noalloc(q_dev.data_ptr(), k_dev.data_ptr(), v_dev.data_ptr(), out_dev.data_ptr(),
-                                        CFG.batch, CFG.q_heads, CFG.kv_heads, CFG.head_dim, max_ctx, pos, stream)
+        rc = L.attention_decode_noalloc(q_dev.data_ptr(), k_dev.data_ptr(), v_dev.data_ptr(), out_dev.data_ptr(), B,
+                                        nq, nkv, hd, max_ctx, cpos, stream)
         assert rc == 0, L.attention_decode_noalloc_error().decode()
-        torch.cuda.synchronize()
-        got = out_dev.cpu().numpy()
+        assert L.attention_decode_noalloc_status(stream) == 0, L.attention_decode_noalloc_error().decode()
+        got = out_dev.cpu().numpy().reshape(B, nq, hd).astype(np.float64)
         assert np.all(np.isfinite(got))
-        err = rel_err(got, ref)
-        assert np.all(err <= TOL_BF16), f"call {call}: error {err.max():.3e} x max|output|"
+        err = np.max(np.abs(got - ref), axis=2) / np.max(np.abs(ref), axis=2)
+        assert np.all(err <= TOL_BF16), f"call {call}: error {err.max():.3e} x max|output| (head {np.argmax(err)})"
+        assert np.array_equal(got[2], np.broadcast_to(synth.bf16_to_f32(v[2, np.arange(nq) // group, 0]), (nq, hd)))
         results.append(got)
         out_dev.fill_(float("nan"))
     assert np.array_equal(results[0], results[1])  # the shared scratch starts clean on every call
@@ -91,8 +83,15 @@ def test_noalloc_refuses_oversized_calls():
     k = torch.zeros(B * nkv * max_ctx * hd, dtype=torch.int16, device="cuda")
     v = torch.zeros(B * nkv * max_ctx * hd, dtype=torch.int16, device="cuda")
     pos = (ctypes.c_int32 * B)(*([P] * B))
+    stream = torch.cuda.current_stream().cuda_stream
     rc = L.attention_decode_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, nq, nkv, hd, max_ctx,
-                                    pos, torch.cuda.current_stream().cuda_stream)
+                                    pos, stream)
     assert rc == lps.LPS_EINVAL
     assert "scratch" in L.attention_decode_noalloc_error().decode()
+    # cache rows past 32-bit coordinates are refused before anything is read
+    rc = L.attention_decode_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), 8, 64, 8, hd,
+                                    1 << 25, pos, stream)
+    assert rc == lps.LPS_EINVAL
+    assert "2^31" in L.attention_decode_noalloc_error().decode()
+    assert L.attention_decode_noalloc_status(stream) == 0
     torch.cuda.synchronize()
