@@ -256,6 +256,7 @@ struct lps_model {
   uint64_t step_count = 0;
   lps_stats stats{};
   bool failed = false;
+  bool alloc_failed = false;  // a device allocation failed (bind gives up; see dev_alloc)
   long long wait_limit = 0;  // device-side wait limit in cycles (0: the kernels' default)
   int attn_max_chunks = 0;
   KTimer timers[7];
@@ -276,7 +277,10 @@ struct lps_pending {
 
 namespace {
 
+// After one allocation has failed, the allocations that follow return nullptr
+// without asking the allocator again (a failed bind stops allocating at once).
 void* dev_alloc(lps_model* m, size_t bytes) {
+  if (m->alloc_failed) return nullptr;
   if (bytes == 0) bytes = 256;
   void* p = nullptr;
   if (m->alloc) {
@@ -285,7 +289,10 @@ void* dev_alloc(lps_model* m, size_t bytes) {
     cudaGetLastError();
     p = nullptr;
   }
-  if (p) m->dev_allocs.push_back(p);
+  if (p)
+    m->dev_allocs.push_back(p);
+  else
+    m->alloc_failed = true;
   return p;
 }
 
@@ -1410,6 +1417,7 @@ extern "C" int model_trace_enable(lps_model* m, int capacity) {
   int rc = model_trace_disable(m);
   if (rc) return rc;
   const size_t bytes = 16 * static_cast<size_t>(capacity);
+  m->alloc_failed = false;
   m->trace_dev = static_cast<unsigned long long*>(dev_alloc(m, bytes));
   if (!m->trace_dev) return fail(LPS_ENOMEM, FN, "trace buffer allocation failed");
   CK(cudaMemset(m->trace_dev, 0, bytes), "cudaMemset");
