@@ -116,6 +116,15 @@ int stage_plan_solve(int n_layers, int n_stages, const uint64_t* layer_bytes, co
                                       [0, pos[b]], so it sees the rows before it in the same step,
                                       and the step returns the logits of every row. The cache calls
                                       (model_kv_export/import) take sequence 0 only. */
+#define LPS_FLAG_PERSISTENT 16u     /* batch 1: run each stage's layers as ONE persistent kernel launch
+                                      per stage and step (a cooperative grid, one CTA per SM, grid-wide
+                                      barriers between the projection and attention phases, all stages
+                                      on one stream) instead of the default chain of per-projection
+                                      kernels. Same results within the oracle tolerance, the same bits
+                                      in every stage plan; on the 8B bf16 step it measures slower than
+                                      the default chain, so it is opt-in. Ignored (stats.persistent = 0)
+                                      for batch > 1, verify rows, the single-stream arm and shapes
+                                      the kernel does not take. */
 #define LPS_FLAG_SERIAL_STEPS 4u   /* make stage 0 of step t+1 also wait for the last stage of step t.
                                       By default stages of consecutive steps overlap, bounded
                                       only by the slot events (tokens t+1.. keep running while
@@ -280,6 +289,8 @@ typedef struct lps_stats {
   uint64_t kernel_launches;    /* this library's kernel launches */
   int n_stages;
   int fence[17];               /* the first min(N, 16)+1 entries of the fence */
+  int persistent;              /* 1: steps run on the persistent stage kernel (LPS_FLAG_PERSISTENT),
+                                  0: the chained per-projection kernels (the default) */
 } lps_stats;
 
 int model_stats(const lps_model* m, lps_stats* out);
@@ -296,8 +307,10 @@ int model_kv_import(lps_model* m, int layer, int b, const void* host, size_t byt
 int model_attn_out(const lps_model* m, int layer, int b, float* host);
 
 /* Per-kernel timing with CUDA events on the launching stream, for the kernel
- * family `kind` (LPS_KERNEL_*). Enabling starts a new measurement; reading
- * synchronizes and returns the summed device time and launch count. */
+ * family `kind` (LPS_KERNEL_QKV .. LPS_KERNEL_STAGE). Enabling starts a new
+ * measurement; reading synchronizes and returns the summed device time and
+ * launch count. A model on the persistent stage kernel launches only
+ * LPS_KERNEL_STAGE; the per-projection families apply to the chained kernels. */
 #define LPS_KERNEL_QKV 0
 #define LPS_KERNEL_ATTN 1
 #define LPS_KERNEL_OPROJ 2
@@ -305,6 +318,8 @@ int model_attn_out(const lps_model* m, int layer, int b, float* host);
 #define LPS_KERNEL_DOWN 4
 #define LPS_KERNEL_HEAD 5
 #define LPS_KERNEL_EMBED 6
+#define LPS_KERNEL_STAGE 7  /* the persistent stage kernel (batch 1): one launch per stage and step */
+#define LPS_KERNEL_MERGE 8  /* trace only: the persistent kernel's merge of the attention chunks */
 int model_time_kernel(lps_model* m, int kind, int enable);
 int model_kernel_time(lps_model* m, int kind, double* total_ms, uint64_t* launches);
 

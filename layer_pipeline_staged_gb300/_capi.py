@@ -22,8 +22,9 @@ LPS_FLAG_SINGLE_STREAM = 1
 LPS_FLAG_KEEP_ATTN_OUT = 2
 LPS_FLAG_SERIAL_STEPS = 4
 LPS_FLAG_VERIFY = 8
+LPS_FLAG_PERSISTENT = 16
 
-KERNELS = {"qkv": 0, "attn": 1, "oproj": 2, "gateup": 3, "down": 4, "head": 5, "embed": 6}
+KERNELS = {"qkv": 0, "attn": 1, "oproj": 2, "gateup": 3, "down": 4, "head": 5, "embed": 6, "stage": 7, "merge": 8}
 
 # every entry point the header declares
 EXPORTS = (
@@ -76,7 +77,8 @@ class TraceRecord(ctypes.Structure):
 class Stats(ctypes.Structure):
     _fields_ = [("steps", ctypes.c_uint64), ("deferred_steps", ctypes.c_uint64), ("stage_walks", ctypes.c_uint64),
                 ("boundary_crossings", ctypes.c_uint64), ("pending_drains", ctypes.c_uint64),
-                ("kernel_launches", ctypes.c_uint64), ("n_stages", ctypes.c_int), ("fence", ctypes.c_int * 17)]
+                ("kernel_launches", ctypes.c_uint64), ("n_stages", ctypes.c_int), ("fence", ctypes.c_int * 17),
+                ("persistent", ctypes.c_int)]
 
 
 _lib = None

@@ -152,6 +152,67 @@ int attn_chunk(int hd, int nkv, int batch, int max_pos, int num_sms);
 int attn_max_chunks(int hd, int nkv, int batch, int max_ctx, int num_sms);
 cudaError_t launch_attention(const AttnParams& p, int batch, int max_pos, cudaStream_t s, bool pdl);
 
+// ---- persistent stage kernel (batch 1) -----------------------------------------
+// One launch runs every layer of a stage (and the embedding on stage 0, the
+// final norm + LM head on the last stage) for one decode step; see stage.cu.
+struct StageLayer {            // one layer's device pointers, in a device table
+  CUtensorMap tmap_k;          // the layer's K cache as a 2D bf16 tensor [nkv*max_ctx rows][hd]
+  CUtensorMap tmap_v;
+  const void* w_qkv;           // packed as for the GEMV (RoPE pairs adjacent)
+  const float* s_qkv;
+  const void* w_o;
+  const float* s_o;
+  const void* w_gu;            // (gate_i, up_i) row pairs
+  const float* s_gu;
+  const void* w_d;
+  const float* s_d;
+  const float* attn_norm;
+  const float* ffn_norm;
+  __nv_bfloat16* kc;           // [nkv][max_ctx][hd]
+  __nv_bfloat16* vc;
+  float* o_out;                // attention output [nq*hd] (the layer's own with LPS_FLAG_KEEP_ATTN_OUT)
+};
+
+struct StageParams {
+  const StageLayer* layers;    // device table [n_layers] of this stage
+  int n_layers;
+  int d, nq, nkv, hd, ffn, vocab, max_ctx;
+  float eps, scale;
+  int pos, tok;                // the step's position; the token when tok_dev is null
+  const int* tok_dev;
+  const void* embed;           // stage 0: the embedding table, else nullptr
+  const float* embed_s;
+  const void* head;            // last stage: the LM head, else nullptr
+  const float* head_s;
+  const float* out_norm;
+  float* logits;               // [vocab]
+  const float* h_in;           // the boundary slot a later stage reads, or nullptr (stage 0)
+  float* h;                    // this stage's residual stream [d]
+  float* h_out;                // where the last layer's down projection writes (next slot, or h)
+  float* q;                    // [nq*hd]
+  float* a;                    // [ffn]
+  float* part;                 // attention chunk partials [nq][nch_max][hd + 4]
+  const float2* rope;          // (cos, sin) table [max_ctx][hd/2]
+  int nch, chunk;              // attention chunks per kv head at this position, positions per chunk
+  int nch_max, nw, depth, xs_bytes, seg_cap;  // set from the plan at launch
+  unsigned long long* bar;     // this stage's grid-barrier counter (monotonic)
+  unsigned long long bar_base; // its value when this launch starts
+  long long wait_limit;        // cycles a wait may take before it reports an error (<= 0: default)
+  int* status;
+  unsigned long long* trace;   // [n_phases][2] trace words of this launch, or nullptr
+};
+
+struct StageKernelPlan {
+  bool ok;                     // the shapes fit the kernel
+  int grid, nw, depth, smem, xs_bytes, seg_cap, nch_max;
+};
+StageKernelPlan stage_kernel_plan(int d, int nq, int nkv, int hd, int ffn, int vocab, bool int8, int num_sms,
+                                  int max_smem);
+void stage_attn_chunks(const StageKernelPlan& g, int hd, int nkv, int pos, int* nch, int* chunk);
+int stage_sub_tile(int hd);  // positions per K/V sub-tile of the stage kernel (its tensor maps' box rows)
+int stage_barriers(const StageParams& p);
+cudaError_t launch_stage(const StageParams& p, bool int8, const StageKernelPlan& plan, cudaStream_t s, bool pdl);
+
 // ---- embedding -------------------------------------------------------------
 struct EmbedParams {
   const void* table;     // [vocab][d] bf16 or int8

@@ -197,6 +197,9 @@ struct StageDev {
   float* out_norm = nullptr;
   GemvPlan plan_qkv{}, plan_o{}, plan_gu{}, plan_d{}, plan_head{};
   SkinnyPlan sk_qkv{}, sk_o{}, sk_gu{}, sk_d{}, sk_head{};  // batch > 1
+  StageLayer* ltab = nullptr;          // persistent kernel: device table of this stage's layers
+  unsigned long long* bar = nullptr;   // persistent kernel: grid-barrier counter
+  uint64_t bar_count = 0;              // grid barriers completed by earlier launches
 };
 
 struct Boundary {
@@ -236,6 +239,8 @@ struct lps_model {
   bool single = false;
   bool skinny = false;  // batch > 1: tensor-core skinny GEMMs on the tiled weight layout
   bool verify = false;  // LPS_FLAG_VERIFY: the batch rows are consecutive positions of one sequence
+  bool persist = false; // batch 1: one persistent stage kernel per stage and step, all on one stream
+  StageKernelPlan skp{};
   lps_alloc_fn alloc = nullptr;
   lps_free_fn free_fn = nullptr;
   void* alloc_ctx = nullptr;
@@ -259,14 +264,14 @@ struct lps_model {
   bool alloc_failed = false;  // a device allocation failed (bind gives up; see dev_alloc)
   long long wait_limit = 0;  // device-side wait limit in cycles (0: the kernels' default)
   int attn_max_chunks = 0;
-  KTimer timers[7];
+  KTimer timers[LPS_KERNEL_STAGE + 1];
   // launch trace: device records [cap][2] (zeroed), host metadata per record
   unsigned long long* trace_dev = nullptr;
   int trace_cap = 0, trace_n = 0;
   uint64_t trace_dropped = 0;
   std::vector<lps_trace_record> trace_meta;
 
-  cudaStream_t stream(int s) const { return single ? st[0].stream : st[s].stream; }
+  cudaStream_t stream(int s) const { return (single || persist) ? st[0].stream : st[s].stream; }
 };
 
 struct lps_pending {
@@ -501,6 +506,19 @@ unsigned long long* trace_slot(lps_model* m, int kind, int stage, int layer) {
   return m->trace_dev + 2 * static_cast<size_t>(m->trace_n++);
 }
 
+// n consecutive trace records (the phases of one persistent launch), or
+// nullptr (all n counted as dropped) when they do not all fit.
+unsigned long long* trace_block(lps_model* m, int n) {
+  if (!m->trace_dev) return nullptr;
+  if (m->trace_n + n > m->trace_cap) {
+    m->trace_dropped += n;
+    return nullptr;
+  }
+  unsigned long long* p = m->trace_dev + 2 * static_cast<size_t>(m->trace_n);
+  m->trace_n += n;
+  return p;
+}
+
 int timer_begin(lps_model* m, int kind, cudaStream_t s, cudaEvent_t* stop) {
   *stop = nullptr;
   KTimer& t = m->timers[kind];
@@ -647,6 +665,9 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
   // verify arm attends one row per launch)
   m->verify = (d.flags & LPS_FLAG_VERIFY) != 0;
   m->attn_max_chunks = attn_max_chunks(hd, nkv, m->verify ? 1 : B, d.max_ctx, m->num_sms);
+  // batch 1, on request: the persistent stage kernel where its shapes fit
+  m->skp = stage_kernel_plan(E, nq, nkv, hd, d.ffn, d.vocab, int8, m->num_sms, max_smem);
+  m->persist = B == 1 && !m->verify && !m->single && (d.flags & LPS_FLAG_PERSISTENT) && m->skp.ok;
 
   // rope table (cos, sin) of angle pos * theta^(-2i/hd), computed in double
   std::vector<float2> rope(static_cast<size_t>(d.max_ctx) * half);
@@ -686,7 +707,8 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
     S.q = static_cast<float*>(dev_alloc(m, sizeof(float) * B * qw));
     S.o = static_cast<float*>(dev_alloc(m, sizeof(float) * B * qw));
     S.a = static_cast<float*>(dev_alloc(m, sizeof(float) * B * d.ffn));
-    S.part = static_cast<float*>(dev_alloc(m, sizeof(float) * B * nq * static_cast<size_t>(m->attn_max_chunks) * (hd + 4)));
+    const size_t part_chunks = m->persist ? static_cast<size_t>(m->skp.nch_max) : static_cast<size_t>(m->attn_max_chunks);
+    S.part = static_cast<float*>(dev_alloc(m, sizeof(float) * B * nq * part_chunks * (hd + 4)));
     S.counter = static_cast<int*>(dev_alloc(m, sizeof(int) * B * nkv));
     S.rope = static_cast<float2*>(dev_alloc(m, sizeof(float2) * rope.size()));
     if (!S.h || !S.q || !S.o || !S.a || !S.part || !S.counter || !S.rope)
@@ -798,6 +820,38 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
       if (!S.out_norm) return bail(LPS_ENOMEM, "allocation failed");
       up.put(S.out_norm, w->out_norm, sizeof(float) * E);
     }
+    if (m->persist) {
+      // the persistent kernel's table of this stage's layers, and its barrier counter
+      std::vector<StageLayer> tab(S.layers.size());
+      for (size_t i = 0; i < S.layers.size(); ++i) {
+        const LayerDev& D = S.layers[i];
+        StageLayer& T = tab[i];
+        // the stage kernel's K/V sub-tiles are shorter than the chained attention's
+        const unsigned long long kv_rows = static_cast<unsigned long long>(seqs) * nkv * d.max_ctx;
+        if (!make_kv_map(&T.tmap_k, D.kc, hd, kv_rows, stage_sub_tile(hd)) ||
+            !make_kv_map(&T.tmap_v, D.vc, hd, kv_rows, stage_sub_tile(hd)))
+          return bail(LPS_ECUDA, "cuTensorMapEncodeTiled failed for the KV cache");
+        T.w_qkv = D.w_qkv;
+        T.s_qkv = D.s_qkv;
+        T.w_o = D.w_o;
+        T.s_o = D.s_o;
+        T.w_gu = D.w_gu;
+        T.s_gu = D.s_gu;
+        T.w_d = D.w_d;
+        T.s_d = D.s_d;
+        T.attn_norm = D.attn_norm;
+        T.ffn_norm = D.ffn_norm;
+        T.kc = D.kc;
+        T.vc = D.vc;
+        T.o_out = D.o_keep ? D.o_keep : S.o;
+      }
+      S.ltab = static_cast<StageLayer*>(dev_alloc(m, sizeof(StageLayer) * tab.size()));
+      S.bar = static_cast<unsigned long long*>(dev_alloc(m, sizeof(unsigned long long)));
+      if (!S.ltab || !S.bar) return bail(LPS_ENOMEM, "stage table allocation failed");
+      up.put(S.ltab, tab.data(), sizeof(StageLayer) * tab.size());
+      if (cudaMemsetAsync(S.bar, 0, sizeof(unsigned long long), S.stream) != cudaSuccess)
+        return bail(LPS_ECUDA, "cudaMemsetAsync failed");
+    }
     up.flush();
     if (up.err != cudaSuccess) return bail(LPS_ECUDA, std::string("upload: ") + cudaGetErrorString(up.err));
     // load barrier: one synchronize per stage (memra_engine::pp, sync_stages_after_load)
@@ -842,6 +896,7 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
   if (e != cudaSuccess) return bail(LPS_ECUDA, std::string("bind: ") + cudaGetErrorString(e));
   m->filled.assign(seqs, 0);
   m->stats.n_stages = N;
+  m->stats.persistent = m->persist ? 1 : 0;
   for (int i = 0; i <= N && i < 17; ++i) m->stats.fence[i] = m->fence[i];
   *out = m;
   return LPS_OK;
@@ -901,9 +956,104 @@ SkinnyParams skinny_params(const lps_model* m, const void* w, const float* wscal
   return p;
 }
 
+// One step on the persistent stage kernel: one launch per stage, in stage
+// order on one stream, chained by programmatic dependent launch; stage s
+// writes its last layer's output into boundary slot [s][step parity] and
+// stage s + 1 reads it from there.
+int enqueue_persistent(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, const int32_t* pos,
+                       float* logits_dev, const char* FN) {
+  const lps_model_desc& d = m->d;
+  const int N = m->N;
+  const int par = static_cast<int>(m->step_count & 1);
+  const cudaStream_t cs = m->st[0].stream;
+  int nch = 1, chunk = 1;
+  stage_attn_chunks(m->skp, d.head_dim, d.n_kv_heads, pos[0], &nch, &chunk);
+  static const int32_t kPhaseKind[] = {LPS_KERNEL_QKV, LPS_KERNEL_ATTN, LPS_KERNEL_MERGE,
+                                       LPS_KERNEL_OPROJ, LPS_KERNEL_GATEUP, LPS_KERNEL_DOWN};
+  for (int s = 0; s < N; ++s) {
+    StageDev& S = m->st[s];
+    StageParams p{};
+    p.layers = S.ltab;
+    p.n_layers = S.l1 - S.l0;
+    p.d = d.n_embd;
+    p.nq = d.n_q_heads;
+    p.nkv = d.n_kv_heads;
+    p.hd = d.head_dim;
+    p.ffn = d.ffn;
+    p.vocab = d.vocab;
+    p.max_ctx = d.max_ctx;
+    p.eps = d.rms_eps;
+    p.scale = 1.0f / std::sqrt(static_cast<float>(d.head_dim));
+    p.pos = pos[0];
+    p.tok = tok_host ? tok_host[0] : 0;
+    p.tok_dev = tok_dev;
+    if (s == 0) {
+      p.embed = S.embed;
+      p.embed_s = S.embed_s;
+    }
+    if (s == N - 1) {
+      p.head = S.head;
+      p.head_s = S.head_s;
+      p.out_norm = S.out_norm;
+      p.logits = logits_dev;
+    }
+    p.h_in = s > 0 ? m->bd[s - 1].slot[par] : nullptr;
+    p.h = S.h;
+    p.h_out = s + 1 < N ? m->bd[s].slot[par] : S.h;
+    p.q = S.q;
+    p.a = S.a;
+    p.part = S.part;
+    p.rope = S.rope;
+    p.nch = nch;
+    p.chunk = chunk;
+    p.bar = S.bar;
+    p.bar_base = S.bar_count * static_cast<unsigned long long>(m->skp.grid);
+    p.wait_limit = m->wait_limit;
+    p.status = m->status_dev;
+    const int nb = stage_barriers(p);
+    const int nph = nb + 1;
+    p.trace = trace_block(m, nph);
+    if (p.trace) {
+      // metadata of the phases, in the kernel's order
+      auto rec = [&](int kind, int layer) {
+        lps_trace_record r{};
+        r.kind = kind;
+        r.stage = s;
+        r.layer = layer;
+        r.step = static_cast<int32_t>(m->step_count);
+        m->trace_meta.push_back(r);
+      };
+      if (s == 0) rec(LPS_KERNEL_EMBED, -1);
+      for (int l = S.l0; l < S.l1; ++l)
+        for (int k : kPhaseKind) rec(k, l);
+      if (s == N - 1) rec(LPS_KERNEL_HEAD, -1);
+    }
+    cudaEvent_t stop;
+    if (timer_begin(m, LPS_KERNEL_STAGE, cs, &stop)) return fail(LPS_ECUDA, FN, "timer event");
+    const cudaError_t e = launch_stage(p, m->int8, m->skp, cs, true);
+    if (e != cudaSuccess) {
+      m->failed = true;
+      return cuda_fail(FN, "stage kernel launch", e);
+    }
+    timer_end(m, LPS_KERNEL_STAGE, cs, stop);
+    S.bar_count += static_cast<uint64_t>(nb);
+    if (s + 1 < N) {
+      ++m->bd[s].steps;
+      ++m->stats.boundary_crossings;
+    }
+    ++m->stats.stage_walks;
+  }
+  m->filled[0] = pos[0] + 1;
+  ++m->step_count;
+  ++m->stats.steps;
+  m->stats.kernel_launches += static_cast<uint64_t>(N);
+  return LPS_OK;
+}
+
 // Enqueue one step; the last stage writes logits_dev [B][V].
 int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, const int32_t* pos, float* logits_dev,
                  const char* FN) {
+  if (m->persist) return enqueue_persistent(m, tok_host, tok_dev, pos, logits_dev, FN);
   const lps_model_desc& d = m->d;
   const int N = m->N, B = d.batch, E = d.n_embd, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads;
   const int qw = nq * hd, half = hd / 2;
@@ -1467,7 +1617,7 @@ extern "C" int model_trace_disable(lps_model* m) {
 }
 
 extern "C" int model_time_kernel(lps_model* m, int kind, int enable) {
-  if (!m || kind < 0 || kind > LPS_KERNEL_EMBED) return fail(LPS_EINVAL, "model_time_kernel", "bad argument");
+  if (!m || kind < 0 || kind > LPS_KERNEL_STAGE) return fail(LPS_EINVAL, "model_time_kernel", "bad argument");
   KTimer& t = m->timers[kind];
   t.on = enable != 0;
   t.used = 0;
@@ -1478,7 +1628,7 @@ extern "C" int model_time_kernel(lps_model* m, int kind, int enable) {
 
 extern "C" int model_kernel_time(lps_model* m, int kind, double* total_ms, uint64_t* launches) {
   static const char* FN = "model_kernel_time";
-  if (!m || kind < 0 || kind > LPS_KERNEL_EMBED || !total_ms || !launches) return fail(LPS_EINVAL, FN, "bad argument");
+  if (!m || kind < 0 || kind > LPS_KERNEL_STAGE || !total_ms || !launches) return fail(LPS_EINVAL, FN, "bad argument");
   int rc = model_synchronize(m);
   if (rc) return rc;
   KTimer& t = m->timers[kind];

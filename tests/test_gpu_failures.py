@@ -125,19 +125,21 @@ def test_bind_fails_closed_on_every_allocation(cfg):
         assert "model_bind" in _capi.load().last_error_string().decode()
 
 
-@pytest.mark.parametrize("batch", [1, 2])
-def test_device_wait_limit_reports_the_kernel(batch):
+@pytest.mark.parametrize("batch,flags,kernel", [(1, lps.LPS_FLAG_PERSISTENT, "persistent stage kernel"), (1, 0, ""),
+                                                (2, 0, "batch > 1")],
+                         ids=["persistent", "chained", "tensor-core"])
+def test_device_wait_limit_reports_the_kernel(batch, flags, kernel):
     cfg = WAITCFG.replace(batch=batch)
     w = synth.make_weights(cfg)
     toks = synth.make_tokens(cfg, 3)
-    m = bind(cfg, w, max_ctx=8)
+    m = bind(cfg, w, max_ctx=8, flags=flags)
     first = m.decode_step(toks[0], 0)
     m.set_wait_limit(1)
     with pytest.raises(lps.LpsError) as ei:
         m.decode_step(toks[1], 1)
     assert ei.value.code == lps.LPS_ECUDA
     msg = str(ei.value)
-    assert "device-side error in" in msg and "timed out" in msg, msg
+    assert "device-side error in" in msg and "timed out" in msg and kernel in msg, msg
     # the model fails closed from now on
     with pytest.raises(lps.LpsError) as ei:
         m.decode_step(toks[1], 1)
@@ -145,7 +147,7 @@ def test_device_wait_limit_reports_the_kernel(batch):
     m.close()
     # the GPU is still usable: a new model computes the same first step and
     # matches the oracle on the next
-    m2 = bind(cfg, w, max_ctx=8)
+    m2 = bind(cfg, w, max_ctx=8, flags=flags)
     assert np.array_equal(m2.decode_step(toks[0], 0), first)
     orc = oracle.Oracle(cfg, w, max_ctx=8)
     orc.step(toks[0], 0)

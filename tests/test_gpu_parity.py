@@ -28,13 +28,18 @@ WIDE_Q8 = WIDE.replace(name="wide_q8", index=99, weight_dtype="int8")
 
 @pytest.mark.parametrize("cfg", [WIDE, WIDE_Q8], ids=lambda c: c.name)
 def test_full_width_layers_match_oracle(cfg):
+    """Both batch-1 paths at the 8B layer width, against the oracle."""
     w = synth.make_weights(cfg)
     T = 6
     toks = synth.make_tokens(cfg, T)
     orc = oracle.Oracle(cfg, w, max_ctx=T)
-    m = bind(cfg, w, max_ctx=T)
-    for t in range(T):
-        assert_close(m.decode_step(toks[t], t), orc.step(toks[t], t), cfg, f"step {t}")
+    ref = [orc.step(toks[t], t) for t in range(T)]
+    for flags in (0, lps.LPS_FLAG_PERSISTENT):
+        m = bind(cfg, w, max_ctx=T, flags=flags)
+        assert m.stats()["persistent"] == (flags != 0)
+        for t in range(T):
+            assert_close(m.decode_step(toks[t], t), ref[t], cfg, f"step {t} (flags {flags})")
+        m.close()
 
 
 @pytest.fixture(scope="module")
@@ -51,25 +56,36 @@ def run_eager(m, toks, start=0):
     return np.stack([m.decode_step(toks[t], start + t) for t in range(len(toks))])
 
 
-def test_tiny_matches_oracle_every_position(tiny):
+# the two batch-1 paths: the chained per-projection kernels (default) and the persistent stage kernel
+ARMS = {"chained": 0, "persistent": lps.LPS_FLAG_PERSISTENT}
+
+
+@pytest.mark.parametrize("arm", ARMS)
+def test_tiny_matches_oracle_every_position(tiny, arm):
     w, toks, ref, _ = tiny
-    m = bind(TINY, w)
+    m = bind(TINY, w, flags=ARMS[arm])
     got = run_eager(m, toks)
-    assert_close(got, ref, TINY, "tiny N=2")
+    assert_close(got, ref, TINY, f"tiny N=2 ({arm})")
     st = m.stats()
+    assert st["persistent"] == (arm == "persistent")
     assert st["stage_walks"] == 2 * len(toks) and st["boundary_crossings"] == len(toks)
     assert st["fence"] == (0, 2, 4)
+    assert st["kernel_launches"] == len(toks) * (2 if arm == "persistent" else 2 + 5 * TINY.n_layers)
 
 
-def test_tiny_stage_plans_bit_identical(tiny):
+@pytest.mark.parametrize("arm", ARMS)
+def test_tiny_stage_plans_bit_identical(tiny, arm):
     w, toks, _, _ = tiny
-    base = run_eager(bind(TINY, w, fence=(0, 4)), toks)
+    base = run_eager(bind(TINY, w, fence=(0, 4), flags=ARMS[arm]), toks)
     for fence in ((0, 2, 4), (0, 1, 2, 3, 4), (0, 3, 4), (0, 1, 4)):
-        m = bind(TINY, w, fence=fence)
+        m = bind(TINY, w, fence=fence, flags=ARMS[arm])
         assert np.array_equal(run_eager(m, toks), base), fence
         assert m.stats()["boundary_crossings"] == (len(fence) - 2) * len(toks)
-    single = bind(TINY, w, fence=(0, 1, 3, 4), flags=lps.LPS_FLAG_SINGLE_STREAM)
-    assert np.array_equal(run_eager(single, toks), base)
+    if arm == "chained":
+        # the single-stream seam (two plain copies per boundary) runs the chained kernels
+        single = bind(TINY, w, fence=(0, 1, 3, 4), flags=lps.LPS_FLAG_SINGLE_STREAM)
+        assert not single.stats()["persistent"]
+        assert np.array_equal(run_eager(single, toks), base)
 
 
 def test_tiny_deferred_pipelined_bit_identical(tiny):

@@ -3,6 +3,7 @@ device start/end times, and no change to the results."""
 import numpy as np
 import pytest
 
+import layer_pipeline_staged_gb300 as lps
 import synth
 from workloads import bind
 
@@ -11,13 +12,22 @@ pytestmark = pytest.mark.gpu
 TINY = synth.CONFIGS["tiny"]
 
 
-def test_trace_records_every_launch_in_order():
+def _per_step(persistent: bool):
+    """Records of one step: one per launch (chained kernels) or one per phase of
+    the persistent stage kernels (with the merge of the attention chunks)."""
+    layer = ["qkv", "attn", "merge", "oproj", "gateup", "down"] if persistent else ["qkv", "attn", "oproj",
+                                                                                     "gateup", "down"]
+    return ["embed"] + layer * TINY.n_layers + ["head"], len(layer)
+
+
+@pytest.mark.parametrize("flags", [lps.LPS_FLAG_PERSISTENT, 0], ids=["persistent", "chained"])
+def test_trace_records_every_launch_in_order(flags):
     w = synth.make_weights(TINY)
     toks = synth.make_tokens(TINY, 3)
-    plain = bind(TINY, w)
+    plain = bind(TINY, w, flags=flags)
     ref = [plain.decode_step(toks[t], t) for t in range(3)]
 
-    m = bind(TINY, w)
+    m = bind(TINY, w, flags=flags)
     m.trace_enable(1024)
     got = [m.decode_step(toks[t], t) for t in range(3)]
     recs, dropped = m.trace_read()
@@ -26,7 +36,7 @@ def test_trace_records_every_launch_in_order():
         assert np.array_equal(a, b)  # tracing changes no result
 
     fence = TINY.fence
-    per_step = ["embed"] + ["qkv", "attn", "oproj", "gateup", "down"] * TINY.n_layers + ["head"]
+    per_step, nl = _per_step(flags != 0)
     assert len(recs) == 3 * len(per_step)
     steps = sorted({r["step"] for r in recs})
     assert len(steps) == 3 and steps == list(range(steps[0], steps[0] + 3))
@@ -34,22 +44,34 @@ def test_trace_records_every_launch_in_order():
         rs = [r for r in recs if r["step"] == steps[t]]
         assert [r["kind"] for r in rs] == per_step
         layers = [r["layer"] for r in rs[1:-1]]
-        assert layers == [l for l in range(TINY.n_layers) for _ in range(5)]
+        assert layers == [l for l in range(TINY.n_layers) for _ in range(nl)]
         for r in rs[1:-1]:
             assert fence[r["stage"]] <= r["layer"] < fence[r["stage"] + 1]
         assert rs[0]["stage"] == 0 and rs[-1]["stage"] == len(fence) - 2
         for r in rs:
             assert 0 < r["start_ns"] <= r["end_ns"]
-        for s in range(len(fence) - 1):  # one stream per stage: its launches start in order
+        for s in range(len(fence) - 1):  # a stage's launches (or phases) start in order
             starts = [r["start_ns"] for r in rs if r["stage"] == s]
             assert starts == sorted(starts)
+        if flags:
+            # phases of one persistent launch are separated by grid barriers: no
+            # phase starts before the previous one has ended on every CTA
+            for a, b in zip(rs, rs[1:]):
+                if a["stage"] == b["stage"]:
+                    assert b["start_ns"] >= a["end_ns"], (a, b)
 
 
-def test_trace_capacity_counts_dropped_launches():
+@pytest.mark.parametrize("flags", [lps.LPS_FLAG_PERSISTENT, 0], ids=["persistent", "chained"])
+def test_trace_capacity_counts_dropped_launches(flags):
     w = synth.make_weights(TINY)
-    m = bind(TINY, w)
-    m.trace_enable(5)
+    m = bind(TINY, w, flags=flags)
+    per_step, _ = _per_step(flags != 0)
+    # the persistent kernel records a launch's phases together or not at all:
+    # room for stage 0's launch only
+    cap = 1 + 6 * TINY.fence[1] + 2 if flags else 5
+    m.trace_enable(cap)
     m.decode_step(synth.make_tokens(TINY, 1)[0], 0)
     recs, dropped = m.trace_read()
-    assert len(recs) == 5 and dropped == 2 + 5 * TINY.n_layers - 5
+    kept = 1 + 6 * TINY.fence[1] if flags else 5
+    assert len(recs) == kept and dropped == len(per_step) - kept
     m.trace_disable()
