@@ -252,6 +252,27 @@ void pending_free(lps_pending* p);
  * model_stream(m, N-1) returns. */
 int decode_step_device(lps_model* m, const int32_t* tokens, const int32_t* pos, float* logits);
 
+/* ---- chunked prefill through the stages -------------------------------- */
+
+/* Prefill (memra_engine::pp, prime_pp_on / prime_pipe_on; ninfer
+ * pipeline-stages.md, "Prefill micro-chunk overlap"): run the n prompt tokens
+ * tokens[0..n) (host int32) of sequence b at positions pos0 .. pos0 + n - 1
+ * through the stages, in chunks of `chunk` tokens (0 = 128, the maximum). Each
+ * chunk's projections run as tcgen05 tensor-core GEMMs over its token rows,
+ * its attention is causal inside the chunk over the cache rows [0, pos], and
+ * the chunk's f32 hidden rows [chunk][n_embd] cross each stage boundary
+ * through two slots ordered by events, so stage s works on chunk c while
+ * stage s + 1 works on chunk c - 1. Writes the KV rows pos0 .. pos0 + n - 1
+ * of every layer; afterwards filled[b] = max(filled[b], pos0 + n), and decode
+ * continues at pos0 + n. logits (host float[vocab], may be NULL) receives the
+ * last prompt token's logits. Returns once the prefill has completed.
+ * Requires a batch-1 model with bf16 weights (the row-major weight layout),
+ * 0 <= pos0 <= filled[b], pos0 + n <= max_ctx and 0 <= tokens[i] < vocab;
+ * else LPS_EINVAL. The first call allocates the prefill buffers (through the
+ * model's allocator; LPS_ENOMEM on failure). Results match the oracle within
+ * the decode tolerance and are the same bits for every stage plan. */
+int model_prefill(lps_model* m, int b, const int32_t* tokens, int n, int pos0, int chunk, float* logits);
+
 /* Block until every stream of the model is idle; reports device-side errors. */
 int model_synchronize(lps_model* m);
 

@@ -212,6 +212,15 @@ class Model:
         _check(load().decode_step_device(self.h, ctypes.c_void_p(tokens_dev_ptr), _ptr(p),
                                          ctypes.c_void_p(logits_dev_ptr)))
 
+    def prefill(self, tokens, pos0: int = 0, b: int = 0, chunk: int = 0, logits: bool = True):
+        """model_prefill: the prompt tokens of sequence b at positions pos0.. in
+        chunks through the stages; returns the last token's logits [vocab] (or None)."""
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32).reshape(-1))
+        out = np.empty(self.V, np.float32) if logits else None
+        _check(load().model_prefill(self.h, int(b), _ptr(t), int(t.size), int(pos0), int(chunk),
+                                    _ptr(out) if logits else None))
+        return out
+
     def synchronize(self):
         _check(load().model_synchronize(self.h))
 
@@ -358,6 +367,10 @@ def pending_wait(p: Pending, timeout_ms: int = -1, out=None) -> np.ndarray:
 
 def pending_free(p: Pending):
     p.free()
+
+
+def model_prefill(model: Model, b: int, tokens, pos0: int = 0, chunk: int = 0, logits: bool = True):
+    return model.prefill(tokens, pos0=pos0, b=b, chunk=chunk, logits=logits)
 
 
 def decode_step_device(model: Model, tokens_dev_ptr: int, pos, logits_dev_ptr: int):

@@ -35,6 +35,7 @@ EXPORTS = (
     "model_time_kernel", "model_kernel_time", "model_set_serial_steps", "attention_decode_noalloc", "attention_decode_noalloc_error",
     "attention_decode_noalloc_scratch_bytes", "model_trace_enable", "model_trace_read", "model_trace_disable",
     "stage_plan_solve", "model_stage_bytes", "model_set_wait_limit", "attention_decode_noalloc_status",
+    "model_prefill",
 )
 
 
@@ -107,6 +108,7 @@ def load(path: str = LIB_PATH):
         "pending_wait": (i, [vp, vp, i]),
         "pending_free": (None, [vp]),
         "decode_step_device": (i, [vp, vp, vp, vp]),
+        "model_prefill": (i, [vp, i, vp, i, i, i, vp]),
         "model_synchronize": (i, [vp]),
         "model_stream": (i, [vp, i, pp]),
         "last_error_string": (ctypes.c_char_p, []),

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "liblps.so")
-SOURCES = ["runtime.cu", "gemv.cu", "attention.cu", "embed.cu", "noalloc.cu", "skinny.cu", "solver.cu", "stage.cu"]
+SOURCES = ["runtime.cu", "gemv.cu", "attention.cu", "embed.cu", "noalloc.cu", "skinny.cu", "solver.cu", "stage.cu", "tcgemm.cu", "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          f"-I{INCLUDE}", f"-I{CSRC}"]

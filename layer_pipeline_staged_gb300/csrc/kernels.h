@@ -152,6 +152,83 @@ int attn_chunk(int hd, int nkv, int batch, int max_pos, int num_sms);
 int attn_max_chunks(int hd, int nkv, int batch, int max_ctx, int num_sms);
 cudaError_t launch_attention(const AttnParams& p, int batch, int max_pos, cudaStream_t s, bool pdl);
 
+// ---- prefill chunk: GEMM on tcgen05 tensor cores ---------------------------------
+// Y[j][r] = sum_k W[r][k] X[j][k] for the ntok token rows of one prefill chunk
+// (token j at position pos0 + j of sequence seq), W the packed bf16 weights
+// [R][K] row-major, X two bf16 planes (hi rows [0, NP), lo rows [NP, 2 NP)).
+// Epilogues: kEpiQkv (RoPE, q [ntok][nq*hd] and the K/V cache rows),
+// kEpiResidual (h[j][r] += y), kEpiSwiglu (a = silu(gate) * up written as the
+// down projection's two bf16 planes xo [2][NP][ldx]).
+struct TcGemmParams {
+  CUtensorMap tmap_w;          // W [R][K] bf16: box 64 x 128, 128-byte swizzle
+  CUtensorMap tmap_x;          // X [2*NP][K] bf16: box 64 x NP, 128-byte swizzle
+  int R, K, NP, ntok, epi;
+  int stages, tmem_cols;       // set from the plan at launch
+  int pos0, seq;
+  float* q;
+  __nv_bfloat16* kc;           // layer cache base [seqs][nkv][max_ctx][hd]
+  __nv_bfloat16* vc;
+  int nq, nkv, hd, max_ctx;
+  const float2* rope;          // [max_ctx][hd/2]
+  float* h;                    // residual rows [ntok][ldh]
+  int ldh;
+  __nv_bfloat16* xo;           // swiglu output planes [2][NP][ldx]
+  int ldx;
+  float* part;                 // scratch [grid][2][NP][128]
+  int* counter;                // scratch [tiles], zero between launches
+  long long wait_limit;
+  int* status;
+  unsigned long long* trace;
+};
+struct TcGemmPlan {
+  int grid, smem, stages, tmem_cols;
+  bool ok;
+};
+constexpr int kTcMaxTokens = 128;  // token rows of one prefill chunk (NP <= 128)
+TcGemmPlan tc_gemm_plan(int NP, int num_sms, int max_smem);
+int tc_gemm_tiles(int R);
+cudaError_t launch_tc_gemm(const TcGemmParams& p, const TcGemmPlan& plan, cudaStream_t s, bool pdl);
+// 2D bf16 tensor map over a row-major [rows][cols] matrix with boxes of 64
+// columns x box_rows rows and the 128-byte swizzle.
+bool make_bf16_map(CUtensorMap* map, const void* base, unsigned long long cols, unsigned long long rows, int box_rows);
+
+// ---- prefill chunk: activation planes and chunk attention ------------------------
+// Rows j < ntok of src [ntok][lds] (RMS-normalised with gain when gain != null)
+// as two bf16 planes x [2][NP][K]: x[j] = bf16(v), x[NP + j] = bf16(v - bf16(v));
+// rows [ntok, NP) of both planes are zeroed.
+struct PrepParams {
+  const float* src;
+  int lds, K, NP, ntok;
+  const float* gain;
+  float eps;
+  __nv_bfloat16* x;
+  unsigned long long* trace;
+};
+cudaError_t launch_prep(const PrepParams& p, cudaStream_t s, bool pdl);
+
+// Causal attention of ntok consecutive tokens (positions pos0 ..) of sequence
+// seq over its cache rows, split by key chunks, then merged into the o-proj
+// activation planes xo [2][NP][nq*hd].
+struct ChunkAttnParams {
+  CUtensorMap tmap_k;          // the layer's cache maps (box 64 x sub-tile rows, 128-byte swizzle)
+  CUtensorMap tmap_v;
+  const float* q;              // [ntok][nq*hd]
+  float* part;                 // [ntok][nq][max_chunks][hd + 4]: o, m, l
+  __nv_bfloat16* xo;
+  int nq, nkv, hd, max_ctx, max_chunks;
+  int chunk, nchunks;          // keys per CTA, CTAs per (block, kv head): chunk_attn_split
+  int seq, pos0, ntok, NP;
+  float scale;
+  long long wait_limit;
+  int* status;
+  unsigned long long* trace;        // attention launch record, or nullptr
+  unsigned long long* trace_merge;  // merge launch record, or nullptr
+};
+int chunk_attn_sub_tile(int hd);
+int chunk_attn_max_chunks(int nkv, int num_sms);
+void chunk_attn_split(int hd, int nkv, int ntok, int pos0, int num_sms, int* nchunks, int* chunk);
+cudaError_t launch_chunk_attn(const ChunkAttnParams& p, cudaStream_t s, bool pdl);
+
 // ---- persistent stage kernel (batch 1) -----------------------------------------
 // One launch runs every layer of a stage (and the embedding on stage 0, the
 // final norm + LM head on the last stage) for one decode step; see stage.cu.

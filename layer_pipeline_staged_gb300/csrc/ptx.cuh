@@ -29,6 +29,9 @@ enum : int {
   kKidAttnCombine = 6, // split-K attention, the last CTA's merge
   kKidEmbed = 7,       // embedding row
   kKidStage = 8,       // the persistent stage kernel
+  kKidTcGemm = 9,      // prefill-chunk GEMM on tcgen05
+  kKidChunkAttn = 10,  // prefill-chunk attention (and its merge)
+  kKidPrep = 11,       // prefill-chunk RMSNorm / split of the activations
   kKidSkinnyBit = 1 << 12,
 };
 

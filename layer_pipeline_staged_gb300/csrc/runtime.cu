@@ -18,6 +18,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <chrono>
 #include <cmath>
 #include <cstdio>
@@ -69,7 +70,10 @@ std::string describe_status(int kinds, int first) {
                                          "split-K attention",
                                          "split-K attention (merge of the chunks)",
                                          "embedding",
-                                         "persistent stage kernel"};
+                                         "persistent stage kernel",
+                                         "prefill GEMM (tcgen05)",
+                                         "prefill chunk attention",
+                                         "prefill RMSNorm / activation split"};
   const int kid = (first >> 8) & 0xf;
   std::string what;
   const int k = first & 0xff ? first & 0xff : kinds;
@@ -79,7 +83,7 @@ std::string describe_status(int kinds, int first) {
   if (k & 8) what += "a kernel argument was out of range; ";
   if (k & 16) what += "a grid-wide barrier wait timed out; ";
   if (what.empty()) what = "unknown error; ";
-  std::string name = kKernels[kid < 9 ? kid : 0];
+  std::string name = kKernels[kid < 12 ? kid : 0];
   if (first & 0x1000) name += " (batch > 1 tensor-core GEMM)";
   char buf[96];
   std::snprintf(buf, sizeof buf, "(status 0x%x, first report 0x%x, detail %d)", kinds, first,
@@ -209,6 +213,30 @@ struct Boundary {
   uint64_t steps = 0;
 };
 
+// Prefill buffers of one stage, allocated at the first model_prefill call
+// (NP = the chunk's token rows padded to 16; C <= kTcMaxTokens).
+struct PrefillStage {
+  float* h = nullptr;               // [C][E] the chunk's residual rows
+  float* q = nullptr;               // [C][nq*hd]
+  __nv_bfloat16* x = nullptr;       // [2][NP][E] planes of the normalised input (QKV, gate/up)
+  __nv_bfloat16* xo = nullptr;      // [2][NP][nq*hd] planes of the attention output (o-proj)
+  __nv_bfloat16* xd = nullptr;      // [2][NP][ffn] planes of the SwiGLU output (down)
+  float* apart = nullptr;           // chunk-attention partials [C][nq][max_chunks][hd + 4]
+  float* gpart = nullptr;           // GEMM partials [grid][2][NP][128]
+  int* gcnt = nullptr;              // GEMM tile counters (zero between launches)
+  int32_t* tok = nullptr;           // stage 0: the prompt's token ids [max_ctx]
+  CUtensorMap map_x{}, map_xo{}, map_xd{};
+  std::vector<CUtensorMap> map_qkv, map_o, map_gu, map_d;  // per layer of the stage
+};
+struct PrefillState {
+  bool ready = false;
+  int C = 0, NP = 0, max_chunks = 0;
+  TcGemmPlan plan{};
+  std::vector<PrefillStage> st;
+  std::vector<Boundary> bd;         // [N-1] boundary slots [C][E], ev_tx / ev_rx per chunk parity
+  uint64_t chunks = 0;              // chunks enqueued (their parity picks the slot)
+};
+
 struct PendingSlot {
   float* logits_dev = nullptr;
   float* host = nullptr;  // pinned [B][V]
@@ -265,6 +293,7 @@ struct lps_model {
   long long wait_limit = 0;  // device-side wait limit in cycles (0: the kernels' default)
   int attn_max_chunks = 0;
   KTimer timers[LPS_KERNEL_STAGE + 1];
+  PrefillState pf;
   // launch trace: device records [cap][2] (zeroed), host metadata per record
   unsigned long long* trace_dev = nullptr;
   int trace_cap = 0, trace_n = 0;
@@ -329,6 +358,11 @@ void release(lps_model* m) {
     if (s.stream) cudaStreamSynchronize(s.stream);
   if (m->rb) cudaStreamSynchronize(m->rb);
   for (auto& b : m->bd)
+    for (int i = 0; i < 2; ++i) {
+      if (b.ev_tx[i]) cudaEventDestroy(b.ev_tx[i]);
+      if (b.ev_rx[i]) cudaEventDestroy(b.ev_rx[i]);
+    }
+  for (auto& b : m->pf.bd)
     for (int i = 0; i < 2; ++i) {
       if (b.ev_tx[i]) cudaEventDestroy(b.ev_tx[i]);
       if (b.ev_rx[i]) cudaEventDestroy(b.ev_rx[i]);
@@ -489,6 +523,27 @@ bool make_kv_map(CUtensorMap* map, void* base, int hd, unsigned long long rows, 
              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+}  // namespace
+
+namespace lps {
+// A row-major [rows][cols] bf16 matrix as a 2D tensor read in boxes of 64
+// columns x box_rows rows with the 128-byte swizzle; reads past either edge
+// give zeros.
+bool make_bf16_map(CUtensorMap* map, const void* base, unsigned long long cols, unsigned long long rows, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), rows};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace lps
+
+namespace {
 
 // The trace record of the next launch (two zeroed 64-bit words), or nullptr.
 unsigned long long* trace_slot(lps_model* m, int kind, int stage, int layer) {
@@ -1333,6 +1388,246 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
   return LPS_OK;
 }
 
+// ---- prefill -------------------------------------------------------------------
+
+// The prefill buffers, boundary slots and tensor maps, at the first prefill call.
+int prefill_init(lps_model* m, const char* FN) {
+  PrefillState& P = m->pf;
+  if (P.ready) return LPS_OK;
+  const lps_model_desc& d = m->d;
+  const int N = m->N, E = d.n_embd, nq = d.n_q_heads, nkv = d.n_kv_heads, hd = d.head_dim, ffn = d.ffn;
+  const int qw = nq * hd, rows_qkv = (nq + 2 * nkv) * hd;
+  int max_smem = 0;
+  CK(cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, m->device), "device attribute");
+  const int C = kTcMaxTokens, NP = kTcMaxTokens;
+  P.plan = tc_gemm_plan(NP, m->num_sms, max_smem);
+  if (!P.plan.ok) return fail(LPS_EINVAL, FN, "the prefill GEMM does not fit this device");
+  P.C = C;
+  P.NP = NP;
+  P.max_chunks = chunk_attn_max_chunks(nkv, m->num_sms);
+  const int max_tiles = tc_gemm_tiles(std::max(std::max(rows_qkv, E), 2 * ffn));
+  P.st.assign(N, PrefillStage{});
+  for (int s = 0; s < N; ++s) {
+    StageDev& S = m->st[s];
+    PrefillStage& F = P.st[s];
+    F.h = static_cast<float*>(dev_alloc(m, sizeof(float) * C * E));
+    F.q = static_cast<float*>(dev_alloc(m, sizeof(float) * C * qw));
+    F.x = static_cast<__nv_bfloat16*>(dev_alloc(m, sizeof(__nv_bfloat16) * 2 * NP * E));
+    F.xo = static_cast<__nv_bfloat16*>(dev_alloc(m, sizeof(__nv_bfloat16) * 2 * NP * qw));
+    F.xd = static_cast<__nv_bfloat16*>(dev_alloc(m, sizeof(__nv_bfloat16) * 2 * NP * ffn));
+    F.apart = static_cast<float*>(dev_alloc(m, sizeof(float) * C * nq * static_cast<size_t>(P.max_chunks) * (hd + 4)));
+    F.gpart = static_cast<float*>(dev_alloc(m, sizeof(float) * P.plan.grid * 2 * NP * 128));
+    F.gcnt = static_cast<int*>(dev_alloc(m, sizeof(int) * max_tiles));
+    if (s == 0) F.tok = static_cast<int32_t*>(dev_alloc(m, sizeof(int32_t) * d.max_ctx));
+    if (!F.h || !F.q || !F.x || !F.xo || !F.xd || !F.apart || !F.gpart || !F.gcnt || (s == 0 && !F.tok))
+      return fail(LPS_ENOMEM, FN, "prefill buffer allocation failed");
+    CK(cudaMemsetAsync(F.gcnt, 0, sizeof(int) * max_tiles, S.stream), "cudaMemsetAsync");
+    CK(cudaMemsetAsync(F.x, 0, sizeof(__nv_bfloat16) * 2 * NP * E, S.stream), "cudaMemsetAsync");
+    CK(cudaMemsetAsync(F.xo, 0, sizeof(__nv_bfloat16) * 2 * NP * qw, S.stream), "cudaMemsetAsync");
+    CK(cudaMemsetAsync(F.xd, 0, sizeof(__nv_bfloat16) * 2 * NP * ffn, S.stream), "cudaMemsetAsync");
+    bool ok = make_bf16_map(&F.map_x, F.x, E, 2 * NP, NP) && make_bf16_map(&F.map_xo, F.xo, qw, 2 * NP, NP) &&
+              make_bf16_map(&F.map_xd, F.xd, ffn, 2 * NP, NP);
+    const size_t nl = S.layers.size();
+    F.map_qkv.resize(nl);
+    F.map_o.resize(nl);
+    F.map_gu.resize(nl);
+    F.map_d.resize(nl);
+    for (size_t i = 0; i < nl && ok; ++i) {
+      const LayerDev& L = S.layers[i];
+      ok = make_bf16_map(&F.map_qkv[i], L.w_qkv, E, rows_qkv, 128) && make_bf16_map(&F.map_o[i], L.w_o, qw, E, 128) &&
+           make_bf16_map(&F.map_gu[i], L.w_gu, E, 2 * ffn, 128) && make_bf16_map(&F.map_d[i], L.w_d, ffn, E, 128);
+    }
+    if (!ok) return fail(LPS_ECUDA, FN, "cuTensorMapEncodeTiled failed for a prefill operand");
+  }
+  P.bd.assign(N > 1 ? N - 1 : 0, Boundary{});
+  for (auto& b : P.bd)
+    for (int i = 0; i < 2; ++i) {
+      b.slot[i] = static_cast<float*>(dev_alloc(m, sizeof(float) * C * E));
+      if (!b.slot[i]) return fail(LPS_ENOMEM, FN, "prefill boundary allocation failed");
+      CK(cudaEventCreateWithFlags(&b.ev_tx[i], cudaEventDisableTiming), "cudaEventCreate");
+      CK(cudaEventCreateWithFlags(&b.ev_rx[i], cudaEventDisableTiming), "cudaEventCreate");
+    }
+  P.ready = true;
+  return LPS_OK;
+}
+
+// Enqueue one chunk: ntok prompt tokens (ids at tok[tok_off..]) of sequence
+// seq at positions pos0 .. pos0 + ntok - 1, through every stage. Stage s waits
+// for stage s - 1's slot of this chunk's parity (ev_tx) and for stage s + 1 to
+// have read its own slot of the same parity two chunks ago (ev_rx), so stage s
+// works on chunk c while stage s + 1 works on chunk c - 1. With want_logits
+// the last stage writes the logits of the chunk's last token.
+int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off, bool want_logits, const char* FN) {
+  PrefillState& P = m->pf;
+  const lps_model_desc& d = m->d;
+  const int N = m->N, E = d.n_embd, nq = d.n_q_heads, nkv = d.n_kv_heads, hd = d.head_dim, ffn = d.ffn;
+  const int qw = nq * hd, NP = P.NP;
+  const int par = static_cast<int>(P.chunks & 1);
+  int nchunks = 1, achunk = 1;
+  chunk_attn_split(hd, nkv, ntok, pos0, m->num_sms, &nchunks, &achunk);
+  uint64_t launches = 0;
+  bool pdl = false;
+#define PF_LAUNCH(call)                                 \
+  do {                                                  \
+    cudaError_t e_ = (call);                            \
+    if (e_ != cudaSuccess) {                            \
+      m->failed = true;                                 \
+      return cuda_fail(FN, "prefill kernel launch", e_); \
+    }                                                   \
+    ++launches;                                         \
+    pdl = true;                                         \
+  } while (0)
+  for (int s = 0; s < N; ++s) {
+    StageDev& S = m->st[s];
+    PrefillStage& F = P.st[s];
+    const cudaStream_t cs = m->stream(s);
+    pdl = false;
+    if (s > 0) CK(cudaStreamWaitEvent(cs, P.bd[s - 1].ev_tx[par], 0), "wait prefill ev_tx");
+    if (s + 1 < N) CK(cudaStreamWaitEvent(cs, P.bd[s].ev_rx[par], 0), "wait prefill ev_rx");
+    if (s == 0) {
+      EmbedParams ep{};
+      ep.table = S.embed;
+      ep.scale = S.embed_s;
+      ep.tok_dev = F.tok + tok_off;
+      ep.d = E;
+      ep.vocab = d.vocab;
+      ep.batch = ntok;
+      ep.h = F.h;
+      ep.status = m->status_dev;
+      PF_LAUNCH(launch_embed(ep, m->int8, cs, pdl));
+    } else {
+      CK(cudaMemcpyAsync(F.h, P.bd[s - 1].slot[par], sizeof(float) * ntok * E, cudaMemcpyDeviceToDevice, cs),
+         "prefill boundary copy");
+      CK(cudaEventRecord(P.bd[s - 1].ev_rx[par], cs), "record prefill ev_rx");
+      pdl = false;
+    }
+    TcGemmParams g{};
+    g.NP = NP;
+    g.ntok = ntok;
+    g.pos0 = pos0;
+    g.seq = seq;
+    g.nq = nq;
+    g.nkv = nkv;
+    g.hd = hd;
+    g.max_ctx = d.max_ctx;
+    g.rope = S.rope;
+    g.h = F.h;
+    g.ldh = E;
+    g.part = F.gpart;
+    g.counter = F.gcnt;
+    g.wait_limit = m->wait_limit;
+    g.status = m->status_dev;
+    PrepParams pp{};
+    pp.src = F.h;
+    pp.lds = E;
+    pp.K = E;
+    pp.NP = NP;
+    pp.ntok = ntok;
+    pp.eps = d.rms_eps;
+    pp.x = F.x;
+    for (int l = S.l0; l < S.l1; ++l) {
+      const int i = l - S.l0;
+      const LayerDev& L = S.layers[i];
+      // RMSNorm -> QKV -> RoPE -> q and the chunk's cache rows
+      pp.gain = L.attn_norm;
+      PF_LAUNCH(launch_prep(pp, cs, pdl));
+      TcGemmParams gq = g;
+      gq.tmap_w = F.map_qkv[i];
+      gq.tmap_x = F.map_x;
+      gq.R = (nq + 2 * nkv) * hd;
+      gq.K = E;
+      gq.epi = kEpiQkv;
+      gq.q = F.q;
+      gq.kc = L.kc;
+      gq.vc = L.vc;
+      PF_LAUNCH(launch_tc_gemm(gq, P.plan, cs, pdl));
+      // causal attention of the chunk, merged into the o-proj input planes
+      ChunkAttnParams ap{};
+      ap.tmap_k = L.tmap_k;
+      ap.tmap_v = L.tmap_v;
+      ap.q = F.q;
+      ap.part = F.apart;
+      ap.xo = F.xo;
+      ap.nq = nq;
+      ap.nkv = nkv;
+      ap.hd = hd;
+      ap.max_ctx = d.max_ctx;
+      ap.max_chunks = P.max_chunks;
+      ap.chunk = achunk;
+      ap.nchunks = nchunks;
+      ap.seq = seq;
+      ap.pos0 = pos0;
+      ap.ntok = ntok;
+      ap.NP = NP;
+      ap.scale = 1.0f / std::sqrt(static_cast<float>(hd));
+      ap.wait_limit = m->wait_limit;
+      ap.status = m->status_dev;
+      PF_LAUNCH(launch_chunk_attn(ap, cs, pdl));
+      ++launches;  // the merge
+      // o-proj + residual
+      TcGemmParams go = g;
+      go.tmap_w = F.map_o[i];
+      go.tmap_x = F.map_xo;
+      go.R = E;
+      go.K = qw;
+      go.epi = kEpiResidual;
+      PF_LAUNCH(launch_tc_gemm(go, P.plan, cs, pdl));
+      // RMSNorm -> gate/up -> SwiGLU (into the down projection's input planes)
+      pp.gain = L.ffn_norm;
+      PF_LAUNCH(launch_prep(pp, cs, pdl));
+      TcGemmParams gg = g;
+      gg.tmap_w = F.map_gu[i];
+      gg.tmap_x = F.map_x;
+      gg.R = 2 * ffn;
+      gg.K = E;
+      gg.epi = kEpiSwiglu;
+      gg.xo = F.xd;
+      gg.ldx = ffn;
+      PF_LAUNCH(launch_tc_gemm(gg, P.plan, cs, pdl));
+      // down + residual
+      TcGemmParams gd = g;
+      gd.tmap_w = F.map_d[i];
+      gd.tmap_x = F.map_xd;
+      gd.R = E;
+      gd.K = ffn;
+      gd.epi = kEpiResidual;
+      PF_LAUNCH(launch_tc_gemm(gd, P.plan, cs, pdl));
+    }
+    if (s + 1 < N) {
+      CK(cudaMemcpyAsync(P.bd[s].slot[par], F.h, sizeof(float) * ntok * E, cudaMemcpyDeviceToDevice, cs),
+         "prefill boundary copy");
+      CK(cudaEventRecord(P.bd[s].ev_tx[par], cs), "record prefill ev_tx");
+      ++m->stats.boundary_crossings;
+    }
+    ++m->stats.stage_walks;
+  }
+  if (want_logits) {
+    // the last token's final RMSNorm -> LM head, on the batch-1 GEMV
+    StageDev& S = m->st[N - 1];
+    const cudaStream_t cs = m->stream(N - 1);
+    GemvParams p{};
+    p.w = S.head;
+    p.wscale = S.head_s;
+    p.rows = d.vocab;
+    p.K = E;
+    p.unit_rows = 1;
+    p.units = d.vocab;
+    p.units_per_buf = S.plan_head.units_per_buf;
+    p.nbuf = S.plan_head.nbuf;
+    p.h = P.st[N - 1].h + static_cast<size_t>(ntok - 1) * E;
+    p.gain = S.out_norm;
+    p.eps = d.rms_eps;
+    p.out = m->eager_logits_dev;
+    p.status = m->status_dev;
+    p.wait_limit = m->wait_limit;
+    PF_LAUNCH(launch_gemv(p, kEpiStore, true, m->int8, S.plan_head, cs, pdl));
+  }
+#undef PF_LAUNCH
+  ++P.chunks;
+  m->stats.kernel_launches += launches;
+  return LPS_OK;
+}
+
 int read_status(lps_model* m, const int* status, const char* FN) {
   if (status[0] != 0 || status[1] != 0) {
     m->failed = true;
@@ -1446,6 +1741,50 @@ extern "C" int decode_step_device(lps_model* m, const int32_t* tokens, const int
   if (!logits) return fail(LPS_EINVAL, FN, "logits is NULL");
   CK(cudaSetDevice(m->device), "cudaSetDevice");
   return enqueue_step(m, nullptr, tokens, pos, logits, FN);
+}
+
+extern "C" int model_prefill(lps_model* m, int b, const int32_t* tokens, int n, int pos0, int chunk,
+                             float* logits) {
+  static const char* FN = "model_prefill";
+  if (!m) return fail(LPS_EINVAL, FN, "model is NULL");
+  if (m->failed) return fail(LPS_ECUDA, FN, "model is in a failed state after an earlier device error");
+  const lps_model_desc& d = m->d;
+  if (m->skinny || m->verify)
+    return fail(LPS_EINVAL, FN, "prefill needs the row-major weight layout of a batch-1 model");
+  if (m->int8) return fail(LPS_EINVAL, FN, "prefill needs bf16 weights");
+  if (!tokens || n < 1) return fail(LPS_EINVAL, FN, "tokens is NULL or n < 1");
+  if (b < 0 || b >= static_cast<int>(m->filled.size())) return fail(LPS_EINVAL, FN, "sequence out of range");
+  if (pos0 < 0 || pos0 > m->filled[b]) return fail(LPS_EINVAL, FN, "pos0 skips unwritten cache rows (pos0 > filled)");
+  if (static_cast<long long>(pos0) + n > d.max_ctx) return fail(LPS_EINVAL, FN, "pos0 + n exceeds max_ctx");
+  if (chunk < 0 || chunk > kTcMaxTokens) return fail(LPS_EINVAL, FN, "chunk out of [0, 128]");
+  for (int i = 0; i < n; ++i)
+    if (tokens[i] < 0 || tokens[i] >= d.vocab)
+      return fail(LPS_EINVAL, FN, "token " + std::to_string(i) + " out of [0, vocab)");
+  const int C = chunk ? chunk : kTcMaxTokens;
+  CK(cudaSetDevice(m->device), "cudaSetDevice");
+  int rc = prefill_init(m, FN);
+  if (rc) return rc;
+  const cudaStream_t first = m->stream(0), last = m->stream(m->N - 1);
+  CK(cudaMemcpyAsync(m->pf.st[0].tok, tokens, sizeof(int32_t) * n, cudaMemcpyHostToDevice, first), "token upload");
+  for (int c0 = 0; c0 < n; c0 += C) {
+    const int ntok = n - c0 < C ? n - c0 : C;
+    rc = enqueue_prefill_chunk(m, b, pos0 + c0, ntok, c0, logits && c0 + ntok == n, FN);
+    if (rc) return rc;
+  }
+  if (pos0 + n > m->filled[b]) m->filled[b] = pos0 + n;
+  const size_t bytes = sizeof(float) * static_cast<size_t>(d.vocab);
+  if (logits) CK(cudaMemcpyAsync(m->eager_host, m->eager_logits_dev, bytes, cudaMemcpyDeviceToHost, last), "logits copy");
+  CK(cudaMemcpyAsync(m->status_host, m->status_dev, 2 * sizeof(int), cudaMemcpyDeviceToHost, last), "status copy");
+  // every stage's last chunk is ordered before the last stage's, so this drains the prefill
+  cudaError_t e = cudaStreamSynchronize(last);
+  if (e != cudaSuccess) {
+    m->failed = true;
+    return cuda_fail(FN, "prefill", e);
+  }
+  rc = read_status(m, m->status_host, FN);
+  if (rc) return rc;
+  if (logits) std::memcpy(logits, m->eager_host, bytes);
+  return LPS_OK;
 }
 
 extern "C" int model_synchronize(lps_model* m) {

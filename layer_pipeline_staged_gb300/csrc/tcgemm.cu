@@ -1,0 +1,458 @@
+// Weight-streaming GEMM on the fifth-generation tensor cores (tcgen05, TMEM
+// accumulators, TMA-fed shared memory) for a block of token rows of one
+// sequence: Y[j][r] = sum_k W[r][k] X[j][k] for j < ntok, with the same fused
+// epilogues as the decode step (RoPE + KV append, residual add, SwiGLU). It
+// runs the projections of a prefill chunk (memra_engine::pp, prime_pp_on /
+// prime_pipe_on: the prompt goes through the same stage split as decode, one
+// micro-chunk of rows at a time).
+//
+// Operands:
+//   - A = the packed weights W [R][K] bf16, row-major (the batch-1 layout, so
+//     no second copy of any matrix), 128-row x 64-column tiles by 2D TMA with
+//     the 128-byte swizzle, which is the canonical K-major layout the MMA reads;
+//   - B = the activations as two bf16 planes, X = hi + lo with hi = bf16(x) and
+//     lo = bf16(x - hi): rows [0, NP) hold hi, rows [NP, 2 NP) lo, so every
+//     activation keeps about 16 significant bits. Each k-step issues two MMAs
+//     (A.hi, A.lo) into the same fp32 accumulator;
+//   - D = 128 weight rows x NP token columns of fp32 in TMEM, two buffers, so
+//     the MMAs of the next tile run while the epilogue drains the last one.
+//
+// Work split (every SM streams the same number of weight bytes): the tiles'
+// k-blocks (tile-major) are cut into gridDim.x equal contiguous ranges, one
+// per CTA. A CTA's range is a sequence of runs, one per tile it touches; a run
+// that covers a whole tile goes straight through the epilogue, a run that
+// covers part of one writes its accumulator to a per-CTA partial slot, and
+// the last CTA to finish a tile adds the tile's partials in k order and runs
+// the epilogue. The split depends only on (R, K, grid), and every sum has a
+// fixed order, so identical inputs give identical bits in every stage plan.
+//
+// Roles: warp 0 lane 0 issues the TMA copies into an S-stage ring (weights
+// of the first stages before the programmatic-dependent-launch wait, as they
+// never depend on the previous kernel); warp 1 allocates TMEM and its lane 0
+// issues the MMAs and the tcgen05.commit arrivals that free ring stages and
+// publish finished accumulators; warps 2..5 (one per 32-lane TMEM quarter)
+// read the accumulators with tcgen05.ld and apply the epilogue. Every wait is
+// bounded and reports through the status word instead of hanging.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace lps {
+namespace {
+
+constexpr int kTM = 128;                 // weight rows per tile (MMA M)
+constexpr int kKB = 64;                  // K elements per k-block: one 128-byte swizzle row
+constexpr int kATile = kTM * kKB * 2;    // bytes of one weight tile
+constexpr int kThreads = 192;            // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kEpiThreads = 128;
+
+// ---- tcgen05 / TMA building blocks ------------------------------------------
+
+__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_2d_hint(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                            uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A . B^T, both operands K-major bf16 in shared memory.
+__device__ __forceinline__ void umma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on `bar` when every MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte
+// swizzled layout: rows of 128 bytes, 8-row groups 1024 bytes apart (the
+// stride byte offset); the leading byte offset is unused for this layout.
+// Bits: start address >> 4 at 0..13, LBO >> 4 at 16..29, SBO >> 4 at 32..45,
+// descriptor version 1 at 46..47, layout type 2 (128-byte swizzle) at 61..63.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr & 0x3ffffu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+// Instruction descriptor of kind::f16: D fp32 (bits 4..5 = 1), A and B bf16
+// (bits 7..9 and 10..12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at
+// bits 17..22, M >> 4 at bits 24..28.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// ---- work split ---------------------------------------------------------------
+
+__device__ __forceinline__ long long range_start(int c, long long T, int G) {
+  return static_cast<long long>(c) * T / G;
+}
+// The CTA whose range holds iteration i: the largest c with range_start(c) <= i.
+__device__ __forceinline__ int owner_of(long long i, long long T, int G) {
+  return static_cast<int>(((i + 1) * G - 1) / T);
+}
+
+struct Run {
+  int tile, k0, k1;  // k-blocks [k0, k1) of tile `tile`
+};
+// Run number `n` of a CTA whose range is [beg, end); false past the last run.
+__device__ __forceinline__ bool run_at(long long beg, long long end, int nkb, int n, Run* r) {
+  if (beg >= end) return false;
+  const long long t0 = beg / nkb;
+  const long long t = t0 + n;
+  const long long lo = t * nkb > beg ? t * nkb : beg;
+  if (lo >= end) return false;
+  const long long hi = (t + 1) * nkb < end ? (t + 1) * nkb : end;
+  r->tile = static_cast<int>(t);
+  r->k0 = static_cast<int>(lo - t * nkb);
+  r->k1 = static_cast<int>(hi - t * nkb);
+  return true;
+}
+
+// ---- epilogue -------------------------------------------------------------------
+
+// Apply the epilogue to one (row, token) value. Rows come in pairs on adjacent
+// lanes (RoPE pairs, gate/up pairs): `other` is the partner row's value.
+__device__ __forceinline__ void epilogue(const TcGemmParams& p, int r, int j, float y, float other) {
+  if (r >= p.R) return;
+  if (p.epi == kEpiResidual) {
+    float* h = p.h + static_cast<size_t>(j) * p.ldh + r;
+    *h = *h + y;
+    return;
+  }
+  const bool odd = r & 1;
+  const float y0 = odd ? other : y, y1 = odd ? y : other;  // the pair's first and second row
+  const int u = r >> 1;
+  if (p.epi == kEpiSwiglu) {
+    if (odd) return;  // the even lane of the pair writes a
+    const float a = y0 / (1.0f + expf(-y0)) * y1;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(a);
+    p.xo[static_cast<size_t>(j) * p.ldx + u] = hi;
+    p.xo[static_cast<size_t>(p.NP + j) * p.ldx + u] = __float2bfloat16_rn(a - __bfloat162float(hi));
+    return;
+  }
+  // kEpiQkv: unit u = (head hh, i) holds rows (hh*hd + i, hh*hd + i + hd/2)
+  const int half = p.hd >> 1;
+  const int hh = u / half, i = u - hh * half;
+  const int pos = p.pos0 + j;
+  float v;
+  int col = i + (odd ? half : 0);
+  if (hh < p.nq + p.nkv) {
+    const float2 cs = p.rope[static_cast<size_t>(pos) * half + i];
+    v = odd ? y0 * cs.y + y1 * cs.x : y0 * cs.x - y1 * cs.y;
+  } else {
+    v = y;
+  }
+  if (hh < p.nq) {
+    p.q[static_cast<size_t>(j) * p.nq * p.hd + hh * p.hd + col] = v;
+  } else {
+    const bool is_k = hh < p.nq + p.nkv;
+    const int g = is_k ? hh - p.nq : hh - p.nq - p.nkv;
+    const size_t row = (static_cast<size_t>(p.seq) * p.nkv + g) * p.max_ctx + pos;
+    (is_k ? p.kc : p.vc)[row * p.hd + col] = __float2bfloat16_rn(v);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcGemmParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment of the tiles (the swizzle pattern repeats every 1024 bytes)
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = p.stages, NP = p.NP;
+  const int btile = NP * 128;  // bytes of one activation plane's k-block
+  const int stage_bytes = kATile + 2 * btile;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * stage_bytes);
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;   // [2]: an accumulator buffer is ready for the epilogue
+  uint64_t* acc_empty = acc_full + 2;  // [2]: the epilogue has drained it
+  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  int* flag = reinterpret_cast<int*>(tmem_base + 1);  // [0]: this CTA finishes the tile
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  trace_start(p.trace);
+  const int G = gridDim.x, c = blockIdx.x;
+  const int ntiles = (p.R + kTM - 1) / kTM, nkb = (p.K + kKB - 1) / kKB;
+  const long long T = static_cast<long long>(ntiles) * nkb;
+  const long long beg = range_start(c, T, G), end = range_start(c + 1, T, G);
+  const long long limit = wait_cycles(p.wait_limit);
+
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kEpiThreads);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_base, p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_base;
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first();
+      const long long n_it = end - beg;
+      const long long pre = n_it < S ? n_it : S;
+      bool ok = true;
+      long long n = 0;
+      // the first stages' weights before the dependency wait
+      for (; n < pre; ++n) {
+        const long long i = beg + n;
+        uint8_t* st = smem + static_cast<size_t>(n) * stage_bytes;
+        mbar_arrive_expect_tx(&full[n], stage_bytes);
+        tma_2d_hint(st, &p.tmap_w, static_cast<int>(i % nkb) * kKB, static_cast<int>(i / nkb) * kTM, &full[n], pol);
+      }
+      pdl_wait();
+      for (long long m = 0; m < pre; ++m) {
+        const long long i = beg + m;
+        uint8_t* st = smem + static_cast<size_t>(m) * stage_bytes;
+        const int x = static_cast<int>(i % nkb) * kKB;
+        tma_2d(st + kATile, &p.tmap_x, x, 0, &full[m]);
+        tma_2d(st + kATile + btile, &p.tmap_x, x, NP, &full[m]);
+      }
+      for (; n < n_it && ok; ++n) {
+        const int s = static_cast<int>(n % S);
+        const uint32_t par = static_cast<uint32_t>((n / S - 1) & 1);
+        if (!mbar_wait(&empty[s], par, limit)) {
+          report_error(p.status, kErrWaitEmpty | (kKidTcGemm << 8));
+          ok = false;
+          break;
+        }
+        const long long i = beg + n;
+        uint8_t* st = smem + static_cast<size_t>(s) * stage_bytes;
+        const int x = static_cast<int>(i % nkb) * kKB;
+        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        tma_2d_hint(st, &p.tmap_w, x, static_cast<int>(i / nkb) * kTM, &full[s], pol);
+        tma_2d(st + kATile, &p.tmap_x, x, 0, &full[s]);
+        tma_2d(st + kATile + btile, &p.tmap_x, x, NP, &full[s]);
+      }
+      // every copy issued lands before the CTA may end
+      for (long long m = n - S < 0 ? 0 : n - S; m < n; ++m)
+        if (!mbar_wait(&full[m % S], static_cast<uint32_t>((m / S) & 1), kDrainLimitCycles)) {
+          report_error(p.status, kErrDrain | (kKidTcGemm << 8));
+          break;
+        }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kTM, NP);
+      long long n = 0;
+      bool ok = true;
+      Run r;
+      for (int ri = 0; ok && run_at(beg, end, nkb, ri, &r); ++ri) {
+        const int b = ri & 1;
+        if (ri >= 2 && !mbar_wait(&acc_empty[b], static_cast<uint32_t>(((ri >> 1) - 1) & 1), limit)) {
+          report_error(p.status, kErrWaitEmpty | (kKidTcGemm << 8) | (1 << 13));
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tbase + static_cast<uint32_t>(b * NP);
+        for (int kb = r.k0; kb < r.k1; ++kb, ++n) {
+          const int s = static_cast<int>(n % S);
+          if (!mbar_wait(&full[s], static_cast<uint32_t>((n / S) & 1), limit)) {
+            report_error(p.status, kErrWaitFull | (kKidTcGemm << 8));
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + static_cast<size_t>(s) * stage_bytes);
+          const uint64_t da = sw128_desc(st), dh = sw128_desc(st + kATile), dl = sw128_desc(st + kATile + btile);
+#pragma unroll
+          for (int kk = 0; kk < kKB / 16; ++kk) {
+            // +32 bytes along the swizzled row per 16-element k-step (>> 4 in the descriptor)
+            const uint64_t adv = static_cast<uint64_t>(2 * kk);
+            umma_bf16(d, da + adv, dh + adv, idesc, (kb > r.k0 || kk > 0) ? 1u : 0u);
+            umma_bf16(d, da + adv, dl + adv, idesc, 1u);
+          }
+          umma_commit(&empty[s]);  // the stage is free once these MMAs have read it
+        }
+        if (!ok) break;
+        umma_commit(&acc_full[b]);
+      }
+    }
+  } else {
+    // ---------------- epilogue: warps 2..5, TMEM lane quarter warp % 4 ----------------
+    const int quarter = warp & 3;
+    const int m = quarter * 32 + lane;  // this thread's row of the tile
+    const int etid = tid - 64;          // 0..127
+    // barrier 1 over the four epilogue warps, and the same with an OR vote
+    auto epi_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); };
+    auto epi_or = [](bool bad) -> bool {
+      uint32_t res;
+      asm volatile(
+          "{\n\t.reg .pred p, q;\n\t"
+          "setp.ne.u32 p, %1, 0;\n\t"
+          "bar.red.or.pred q, 1, %2, p;\n\t"
+          "selp.u32 %0, 1, 0, q;\n\t}"
+          : "=r"(res)
+          : "r"(static_cast<uint32_t>(bad)), "n"(kEpiThreads)
+          : "memory");
+      return res != 0;
+    };
+    pdl_wait();                         // residuals and caches of earlier kernels are visible
+    Run r;
+    for (int ri = 0; run_at(beg, end, nkb, ri, &r); ++ri) {
+      const int b = ri & 1;
+      const bool got = mbar_wait(&acc_full[b], static_cast<uint32_t>((ri >> 1) & 1), limit);
+      if (!got && lane == 0) report_error(p.status, kErrWaitFull | (kKidTcGemm << 8) | (2 << 13));
+      if (epi_or(!got)) break;  // the four warps leave together
+      tc_fence_after();
+      const uint32_t tacc = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(b * NP);
+      const bool whole = r.k0 == 0 && r.k1 == nkb;
+      const int row = r.tile * kTM + m;
+      // partial slot of this CTA: 0 for its first run, 1 for its last
+      float* slot = p.part + (static_cast<size_t>(c) * 2 + (ri == 0 ? 0 : 1)) * static_cast<size_t>(NP) * kTM;
+      for (int c0 = 0; c0 < NP; c0 += 16) {
+        float v[16];
+        tmem_ld16(tacc + static_cast<uint32_t>(c0), v);
+        if (whole) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float other = __shfl_xor_sync(0xffffffffu, v[e], 1);
+            if (c0 + e < p.ntok) epilogue(p, row, c0 + e, v[e], other);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) slot[static_cast<size_t>(c0 + e) * kTM + m] = v[e];
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[b]);
+      if (whole) continue;
+      // a partial: publish it; the last CTA of the tile to do so finishes the tile
+      __threadfence();
+      epi_sync();
+      const long long t0i = static_cast<long long>(r.tile) * nkb, t1i = t0i + nkb - 1;
+      const int cf = owner_of(t0i, T, G), cl = owner_of(t1i, T, G);
+      if (etid == 0) {
+        int contributors = 0;  // CTAs with a non-empty range inside the tile
+        for (int cc = cf; cc <= cl; ++cc) contributors += range_start(cc, T, G) < range_start(cc + 1, T, G);
+        const int prev = atomicAdd(p.counter + r.tile, 1);
+        flag[0] = prev == contributors - 1;
+      }
+      epi_sync();
+      if (!flag[0]) continue;
+      __threadfence();
+      for (int j = 0; j < NP; ++j) {
+        float y = 0.f;
+        for (int cc = cf; cc <= cl; ++cc) {
+          const long long s0 = range_start(cc, T, G);
+          if (s0 >= range_start(cc + 1, T, G)) continue;  // an empty range wrote nothing
+          // the tile is CTA cc's first run unless cc started in an earlier tile
+          const int si = s0 < t0i ? 1 : 0;
+          y += __ldcg(p.part + ((static_cast<size_t>(cc) * 2 + si) * NP + j) * kTM + m);
+        }
+        const float other = __shfl_xor_sync(0xffffffffu, y, 1);
+        if (j < p.ntok) epilogue(p, row, j, y, other);
+      }
+      if (etid == 0) p.counter[r.tile] = 0;
+    }
+  }
+
+  trace_end(p.trace);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, p.tmem_cols);
+  }
+}
+
+}  // namespace
+
+int tc_gemm_tiles(int R) { return (R + kTM - 1) / kTM; }
+
+// Ring depth from the shared memory: one stage is a 16 KB weight tile and the
+// two activation planes of the same k-block (NP rows of 128 bytes each).
+TcGemmPlan tc_gemm_plan(int NP, int num_sms, int max_smem) {
+  TcGemmPlan g{};
+  if (NP < 16 || NP > kTcMaxTokens || NP % 16) return g;
+  const int stage = kATile + 2 * NP * 128;
+  const int fixed = 1024 + 64 * 8 + 16;  // alignment slack, barriers, TMEM address and flags
+  int stages = (max_smem - fixed) / stage;
+  stages = stages > 8 ? 8 : stages;
+  if (stages < 2) return g;
+  int cols = 32;
+  while (cols < 2 * NP) cols *= 2;
+  g.grid = num_sms;
+  g.stages = stages;
+  g.smem = stages * stage + fixed;
+  g.tmem_cols = cols;
+  g.ok = true;
+  return g;
+}
+
+cudaError_t launch_tc_gemm(const TcGemmParams& p, const TcGemmPlan& plan, cudaStream_t s, bool pdl) {
+  static std::atomic<int> smem_set[kMaxDevices];
+  cudaError_t e = set_smem_attr(tc_gemm_kernel, plan.smem, smem_set);
+  if (e != cudaSuccess) return e;
+  TcGemmParams q = p;
+  q.stages = plan.stages;
+  q.tmem_cols = plan.tmem_cols;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = plan.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel, q);
+}
+
+}  // namespace lps
