@@ -9,8 +9,9 @@ Default workload: the 8B-shape decoder (32 layers, n_embd 4096, 32 q / 8 kv
 heads, head_dim 128, ffn 14336, vocab 128256), bf16 weights and KV cache,
 batch 1, 4 stages (cuts 8, 16, 24), context 8192, 256 decode steps, deferred
 logits readback. Weights are seeded N(0, 0.02) (synthetic: no checkpoint);
-the context's cache rows are filled synthetically (their values do not change
-the time); the weights (15 GB) are far larger than L2, so every step streams
+the context's cache rows are written by the chunked prefill of a seeded prompt
+(model_prefill, timed and reported as "prefill"; int8 and batch > 1 workloads
+fill them synthetically, as their values do not change the step time); the weights (15 GB) are far larger than L2, so every step streams
 them from HBM.
 
 Prints one JSON line. ``--impl reference`` times the CPU oracle on the same
@@ -46,7 +47,10 @@ def parse():
     ap.add_argument("--ctx", type=int, default=None, help="context length before the timed steps")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--fill", default="synthetic", choices=["synthetic", "decode"])
+    ap.add_argument("--fill", default="auto", choices=["auto", "prefill", "synthetic", "decode"],
+                    help="how the context rows before the timed steps are written: model_prefill (chunked "
+                         "prefill through the stages, timed and reported), synthetic rows, or decode steps; "
+                         "auto = prefill where the model takes it (batch 1, bf16 weights), else synthetic")
     ap.add_argument("--serial", action="store_true", help="no overlap between consecutive steps' stages")
     ap.add_argument("--stages", type=int, default=0,
                     help="even split into this many stages instead of the workload's own cuts (0 = the workload's)")
@@ -303,8 +307,30 @@ def main():
     toks = synth.make_tokens(cfg, W + K)
     start = ctx - W * adv
     seqs = 1 if M else B  # sequences with a cache of their own
-    # context rows [0, start): synthetic cache contents, or teacher-forced decode steps
-    if args.fill == "synthetic" and start > 0:
+    # context rows [0, start): the chunked prefill of a seeded prompt, synthetic
+    # cache contents, or teacher-forced decode steps
+    fill = args.fill
+    if fill == "auto":
+        fill = "prefill" if (B == 1 and not M and cfg.weight_dtype == "bf16") else "synthetic"
+    prefill_info = None
+    if fill == "prefill" and start > 0:
+        ptoks = synth.make_tokens(cfg, start, seed=cfg.seed_t + 9)
+        model.prefill(ptoks[:min(start, 128)], logits=False)  # allocates the prefill buffers (untimed)
+        pf_s = []
+        for _ in range(2):
+            t0 = time.perf_counter()
+            model.prefill(ptoks, logits=True)
+            pf_s.append(time.perf_counter() - t0)
+        pf = min(pf_s)
+        layer_params = (cfg.n_embd * (cfg.q_heads + 2 * cfg.kv_heads) * cfg.head_dim
+                        + cfg.q_heads * cfg.head_dim * cfg.n_embd + 3 * cfg.n_embd * cfg.ffn)
+        flops = 2.0 * start * layer_params * cfg.n_layers
+        prefill_info = {"tokens": start, "chunk": 128, "seconds": pf, "tokens_per_s": start / pf,
+                        "projection_tflops": flops / pf / 1e12,
+                        "how": "model_prefill of the seeded prompt (positions 0..ctx-1, chunks of 128 through "
+                               "the stages), host wall time of the synchronous call, best of 2; "
+                               "projection_tflops counts 2 x tokens x projection weights (attention excluded)"}
+    elif fill == "synthetic" and start > 0:
         for l in range(cfg.n_layers):
             for b in range(seqs):
                 k = synth.uniform_bf16(cfg.seed_t + 5, 2 * (l * B + b), (cfg.kv_heads, max_ctx, cfg.head_dim))
@@ -440,7 +466,7 @@ def main():
         "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": dtype_of(cfg), "data": "synthetic",
         "config": {"workload": wl, "l2": "inputs larger than L2 (every step streams all weights from HBM)",
-                   "cache_fill": args.fill, "steps_overlap": not args.serial,
+                   "cache_fill": fill, "steps_overlap": not args.serial,
                    "parallelism": f"{plan.n_stages} stages on one device"
                    + (f", {n} independent replicas" if n > 1 else "")},
         "hbm_gbs": hbm_gbs, "hbm_frac_of_8tbs": hbm_gbs / NOMINAL_HBM_GBS,
@@ -468,6 +494,8 @@ def main():
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    if prefill_info:
+        line["prefill"] = prefill_info
     if rank == 0:
         print(json.dumps(line), flush=True)
     model.close()

@@ -30,6 +30,7 @@ namespace {
 
 constexpr int kPrepThreads = 256;
 constexpr int kRing = 3;
+constexpr int kMaxMergeChunks = 320;  // key chunks per token the merge takes (chunk_attn_max_chunks)
 
 // ---- activation planes --------------------------------------------------------
 
@@ -342,32 +343,44 @@ __global__ void __launch_bounds__(256) chunk_attn_kernel(const __grid_constant__
 }
 
 // Token j: combine its key chunks in chunk order and write the o-projection's
-// activation planes xo[j] = bf16(o), xo[NP + j] = bf16(o - bf16(o)).
+// activation planes xo[j] = bf16(o), xo[NP + j] = bf16(o - bf16(o)). Warp w
+// takes heads w, w + 8, ...: the chunks' weights exp(m_c - M) once per head
+// (lane c, c + 32, ...; then fixed warp trees), then every dimension's sum
+// over the chunks in chunk order.
 template <int HD>
 __global__ void __launch_bounds__(256) chunk_merge_kernel(const __grid_constant__ ChunkAttnParams p) {
+  __shared__ float wsm[8][kMaxMergeChunks];
   trace_start(p.trace);
   pdl_launch_dependents();
   pdl_wait();
-  const int j = blockIdx.x, qw = p.nq * HD;
+  const int j = blockIdx.x, qw = p.nq * HD, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j0 = (j / 16) * 16, jn = min(16, p.ntok - j0);
   const int kend = p.pos0 + j0 + jn;
   const int nch = (kend + p.chunk - 1) / p.chunk;
-  for (int idx = threadIdx.x; idx < qw; idx += blockDim.x) {
-    const int h = idx / HD, d = idx - h * HD;
+  for (int h = warp; h < p.nq; h += 8) {
     const float* base = p.part + (static_cast<size_t>(j) * p.nq + h) * p.max_chunks * (HD + 4);
-    float M = -INFINITY;
-    for (int c = 0; c < nch; ++c) M = fmaxf(M, base[c * (HD + 4) + HD]);
-    float L = 0.f, O = 0.f;
-    for (int c = 0; c < nch; ++c) {
-      const float* pc = base + c * (HD + 4);
-      const float w = pc[HD] == -INFINITY ? 0.f : expf(pc[HD] - M);
-      L += pc[HD + 1] * w;
-      O += pc[d] * w;
+    float mloc = -INFINITY;
+    for (int c = lane; c < nch; c += 32) mloc = fmaxf(mloc, base[c * (HD + 4) + HD]);
+    const float M = warp_max(mloc);
+    float lloc = 0.f;
+    for (int c = lane; c < nch; c += 32) {
+      const float mc = base[c * (HD + 4) + HD];
+      const float wc = mc == -INFINITY ? 0.f : expf(mc - M);
+      wsm[warp][c] = wc;
+      lloc += base[c * (HD + 4) + HD + 1] * wc;
     }
-    const float o = O / L;
-    const __nv_bfloat16 hi = __float2bfloat16_rn(o);
-    p.xo[static_cast<size_t>(j) * qw + idx] = hi;
-    p.xo[static_cast<size_t>(p.NP + j) * qw + idx] = __float2bfloat16_rn(o - __bfloat162float(hi));
+    const float L = warp_sum(lloc);
+    __syncwarp();
+    for (int d = lane; d < HD; d += 32) {
+      float O = 0.f;
+      for (int c = 0; c < nch; ++c) O += base[c * (HD + 4) + d] * wsm[warp][c];
+      const float o = O / L;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(o);
+      const size_t idx = static_cast<size_t>(h) * HD + d;
+      p.xo[static_cast<size_t>(j) * qw + idx] = hi;
+      p.xo[static_cast<size_t>(p.NP + j) * qw + idx] = __float2bfloat16_rn(o - __bfloat162float(hi));
+    }
+    __syncwarp();
   }
   trace_end(p.trace);
 }
@@ -432,7 +445,8 @@ void chunk_attn_split(int hd, int nkv, int ntok, int pos0, int num_sms, int* nch
 }
 
 cudaError_t launch_chunk_attn(const ChunkAttnParams& p, cudaStream_t s, bool pdl) {
-  if (p.nq % p.nkv || p.nq / p.nkv > 8 || p.nq / p.nkv < 1 || p.ntok < 1 || p.ntok > kTcMaxTokens)
+  if (p.nq % p.nkv || p.nq / p.nkv > 8 || p.nq / p.nkv < 1 || p.ntok < 1 || p.ntok > kTcMaxTokens ||
+      p.max_chunks > kMaxMergeChunks || p.nchunks > p.max_chunks)
     return cudaErrorInvalidValue;
   if (p.hd == 128) return launch_chunk_attn_t<128>(p, s, pdl);
   if (p.hd == 64) return launch_chunk_attn_t<64>(p, s, pdl);

@@ -30,8 +30,9 @@
 // of the first stages before the programmatic-dependent-launch wait, as they
 // never depend on the previous kernel); warp 1 allocates TMEM and its lane 0
 // issues the MMAs and the tcgen05.commit arrivals that free ring stages and
-// publish finished accumulators; warps 2..5 (one per 32-lane TMEM quarter)
-// read the accumulators with tcgen05.ld and apply the epilogue. Every wait is
+// publish finished accumulators; warps 2..9 (two per 32-lane TMEM quarter,
+// each taking half of the token columns) read the accumulators with
+// tcgen05.ld and apply the epilogue. Every wait is
 // bounded and reports through the status word instead of hanging.
 #include "kernels.h"
 #include "ptx.cuh"
@@ -42,8 +43,8 @@ namespace {
 constexpr int kTM = 128;                 // weight rows per tile (MMA M)
 constexpr int kKB = 64;                  // K elements per k-block: one 128-byte swizzle row
 constexpr int kATile = kTM * kKB * 2;    // bytes of one weight tile
-constexpr int kThreads = 192;            // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int kEpiThreads = 128;
+constexpr int kThreads = 320;            // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int kEpiThreads = 256;
 
 // ---- tcgen05 / TMA building blocks ------------------------------------------
 
@@ -153,45 +154,71 @@ __device__ __forceinline__ bool run_at(long long beg, long long end, int nkb, in
 
 // ---- epilogue -------------------------------------------------------------------
 
-// Apply the epilogue to one (row, token) value. Rows come in pairs on adjacent
-// lanes (RoPE pairs, gate/up pairs): `other` is the partner row's value.
-__device__ __forceinline__ void epilogue(const TcGemmParams& p, int r, int j, float y, float other) {
-  if (r >= p.R) return;
+// Apply the epilogue to 16 consecutive token columns [j0, j0 + 16) of one
+// row. Rows come in pairs on adjacent lanes (RoPE pairs, gate/up pairs):
+// w[e] is the partner row's value of column j0 + e. Every load of the group
+// (residual rows, RoPE angles) is issued before its first store, so a group
+// costs one memory round trip, not sixteen.
+__device__ __forceinline__ void epilogue16(const TcGemmParams& p, int r, int j0, const float* v, const float* w) {
+  const int nj = p.ntok - j0;
+  if (r >= p.R || nj <= 0) return;
   if (p.epi == kEpiResidual) {
-    float* h = p.h + static_cast<size_t>(j) * p.ldh + r;
-    *h = *h + y;
+    float* h = p.h + static_cast<size_t>(j0) * p.ldh + r;
+    float in[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) in[e] = e < nj ? h[static_cast<size_t>(e) * p.ldh] : 0.f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      if (e < nj) h[static_cast<size_t>(e) * p.ldh] = in[e] + v[e];
     return;
   }
   const bool odd = r & 1;
-  const float y0 = odd ? other : y, y1 = odd ? y : other;  // the pair's first and second row
   const int u = r >> 1;
   if (p.epi == kEpiSwiglu) {
     if (odd) return;  // the even lane of the pair writes a
-    const float a = y0 / (1.0f + expf(-y0)) * y1;
-    const __nv_bfloat16 hi = __float2bfloat16_rn(a);
-    p.xo[static_cast<size_t>(j) * p.ldx + u] = hi;
-    p.xo[static_cast<size_t>(p.NP + j) * p.ldx + u] = __float2bfloat16_rn(a - __bfloat162float(hi));
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      if (e >= nj) break;
+      const float g = v[e], up = w[e];
+      const float a = g / (1.0f + expf(-g)) * up;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(a);
+      p.xo[static_cast<size_t>(j0 + e) * p.ldx + u] = hi;
+      p.xo[static_cast<size_t>(p.NP + j0 + e) * p.ldx + u] = __float2bfloat16_rn(a - __bfloat162float(hi));
+    }
     return;
   }
   // kEpiQkv: unit u = (head hh, i) holds rows (hh*hd + i, hh*hd + i + hd/2)
   const int half = p.hd >> 1;
   const int hh = u / half, i = u - hh * half;
-  const int pos = p.pos0 + j;
-  float v;
-  int col = i + (odd ? half : 0);
+  const int col = i + (odd ? half : 0);
+  float out[16];
   if (hh < p.nq + p.nkv) {
-    const float2 cs = p.rope[static_cast<size_t>(pos) * half + i];
-    v = odd ? y0 * cs.y + y1 * cs.x : y0 * cs.x - y1 * cs.y;
+    float2 cs[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      cs[e] = e < nj ? p.rope[static_cast<size_t>(p.pos0 + j0 + e) * half + i] : make_float2(1.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float y0 = odd ? w[e] : v[e], y1 = odd ? v[e] : w[e];  // the pair's first and second row
+      out[e] = odd ? y0 * cs[e].y + y1 * cs[e].x : y0 * cs[e].x - y1 * cs[e].y;
+    }
   } else {
-    v = y;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) out[e] = v[e];
   }
   if (hh < p.nq) {
-    p.q[static_cast<size_t>(j) * p.nq * p.hd + hh * p.hd + col] = v;
+    float* q = p.q + static_cast<size_t>(j0) * p.nq * p.hd + hh * p.hd + col;
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      if (e < nj) q[static_cast<size_t>(e) * p.nq * p.hd] = out[e];
   } else {
     const bool is_k = hh < p.nq + p.nkv;
     const int g = is_k ? hh - p.nq : hh - p.nq - p.nkv;
-    const size_t row = (static_cast<size_t>(p.seq) * p.nkv + g) * p.max_ctx + pos;
-    (is_k ? p.kc : p.vc)[row * p.hd + col] = __float2bfloat16_rn(v);
+    __nv_bfloat16* c = (is_k ? p.kc : p.vc) +
+                       ((static_cast<size_t>(p.seq) * p.nkv + g) * p.max_ctx + p.pos0 + j0) * p.hd + col;
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      if (e < nj) c[static_cast<size_t>(e) * p.hd] = __float2bfloat16_rn(out[e]);
   }
 }
 
@@ -324,11 +351,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       }
     }
   } else {
-    // ---------------- epilogue: warps 2..5, TMEM lane quarter warp % 4 ----------------
+    // ---------------- epilogue: warps 2..9 ----------------
+    // warp w reads TMEM lane quarter w % 4 (the hardware's rule) and the
+    // token columns of half (w - 2) / 4 of the accumulator
     const int quarter = warp & 3;
     const int m = quarter * 32 + lane;  // this thread's row of the tile
-    const int etid = tid - 64;          // 0..127
-    // barrier 1 over the four epilogue warps, and the same with an OR vote
+    const int etid = tid - 64;          // 0..255
+    const int cbeg = ((warp - 2) >> 2) * (NP >> 1), cend = cbeg + (NP >> 1);
+    // barrier 1 over the eight epilogue warps, and the same with an OR vote
     auto epi_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); };
     auto epi_or = [](bool bad) -> bool {
       uint32_t res;
@@ -348,22 +378,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const int b = ri & 1;
       const bool got = mbar_wait(&acc_full[b], static_cast<uint32_t>((ri >> 1) & 1), limit);
       if (!got && lane == 0) report_error(p.status, kErrWaitFull | (kKidTcGemm << 8) | (2 << 13));
-      if (epi_or(!got)) break;  // the four warps leave together
+      if (epi_or(!got)) break;  // the epilogue warps leave together
       tc_fence_after();
       const uint32_t tacc = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(b * NP);
       const bool whole = r.k0 == 0 && r.k1 == nkb;
       const int row = r.tile * kTM + m;
       // partial slot of this CTA: 0 for its first run, 1 for its last
       float* slot = p.part + (static_cast<size_t>(c) * 2 + (ri == 0 ? 0 : 1)) * static_cast<size_t>(NP) * kTM;
-      for (int c0 = 0; c0 < NP; c0 += 16) {
-        float v[16];
+      for (int c0 = cbeg; c0 < cend; c0 += 16) {
+        float v[16], w[16];
         tmem_ld16(tacc + static_cast<uint32_t>(c0), v);
         if (whole) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float other = __shfl_xor_sync(0xffffffffu, v[e], 1);
-            if (c0 + e < p.ntok) epilogue(p, row, c0 + e, v[e], other);
-          }
+          for (int e = 0; e < 16; ++e) w[e] = __shfl_xor_sync(0xffffffffu, v[e], 1);
+          epilogue16(p, row, c0, v, w);
         } else {
 #pragma unroll
           for (int e = 0; e < 16; ++e) slot[static_cast<size_t>(c0 + e) * kTM + m] = v[e];
@@ -386,17 +414,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       epi_sync();
       if (!flag[0]) continue;
       __threadfence();
-      for (int j = 0; j < NP; ++j) {
-        float y = 0.f;
+      for (int c0 = cbeg; c0 < cend; c0 += 16) {
+        // the contributors' partials of 16 columns, added in k order
+        float y[16], w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) y[e] = 0.f;
         for (int cc = cf; cc <= cl; ++cc) {
           const long long s0 = range_start(cc, T, G);
           if (s0 >= range_start(cc + 1, T, G)) continue;  // an empty range wrote nothing
           // the tile is CTA cc's first run unless cc started in an earlier tile
           const int si = s0 < t0i ? 1 : 0;
-          y += __ldcg(p.part + ((static_cast<size_t>(cc) * 2 + si) * NP + j) * kTM + m);
+          const float* src = p.part + ((static_cast<size_t>(cc) * 2 + si) * NP + c0) * kTM + m;
+          float t[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) t[e] = __ldcg(src + static_cast<size_t>(e) * kTM);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) y[e] += t[e];
         }
-        const float other = __shfl_xor_sync(0xffffffffu, y, 1);
-        if (j < p.ntok) epilogue(p, row, j, y, other);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = __shfl_xor_sync(0xffffffffu, y[e], 1);
+        epilogue16(p, row, c0, y, w);
       }
       if (etid == 0) p.counter[r.tile] = 0;
     }
@@ -419,7 +456,7 @@ int tc_gemm_tiles(int R) { return (R + kTM - 1) / kTM; }
 // two activation planes of the same k-block (NP rows of 128 bytes each).
 TcGemmPlan tc_gemm_plan(int NP, int num_sms, int max_smem) {
   TcGemmPlan g{};
-  if (NP < 16 || NP > kTcMaxTokens || NP % 16) return g;
+  if (NP < 32 || NP > kTcMaxTokens || NP % 32) return g;
   const int stage = kATile + 2 * NP * 128;
   const int fixed = 1024 + 64 * 8 + 16;  // alignment slack, barriers, TMEM address and flags
   int stages = (max_smem - fixed) / stage;
