@@ -414,7 +414,7 @@ def main():
         # stream (same steps again). Persistent path: the stage kernel, whose launches
         # together carry every byte of the step. Chained path: the kernel family with the
         # most bytes, stages serialized so that no other stage's kernels run beside it
-        # (verify rows launch the attention once per row, batch 1 each).
+        # (verify rows: one causal chunk-attention launch, with its merge, per layer).
         if persistent:
             dom = "stage"
             model.time_kernel(dom, True)
@@ -425,10 +425,14 @@ def main():
             per_launch = {dom: pass_bytes / max(dom_n, 1)}
             per_step = {dom: pass_bytes / K}
         else:
-            attn_cfg = cfg.replace(batch=1) if M else cfg
             pos_mid = ctx + (K // 2) * adv
-            per_launch = {k: kernel_bytes(attn_cfg if k == "attn" else cfg, k, pos_mid) for k in ("gateup", "attn")}
-            per_step = {k: per_launch[k] * (M if (M and k == "attn") else 1) * cfg.n_layers for k in per_launch}
+            per_launch = {k: kernel_bytes(cfg, k, pos_mid) for k in ("gateup", "attn")}
+            if M:
+                # verify rows: one causal chunk-attention launch reads the sequence's
+                # rows [0, pos + M) once for all M rows
+                qw = cfg.q_heads * cfg.head_dim
+                per_launch["attn"] = kernel_bytes(cfg.replace(batch=1), "attn", pos_mid + M - 1) + 2 * (M - 1) * qw * 4
+            per_step = {k: per_launch[k] * cfg.n_layers for k in per_launch}
             dom = max(per_step, key=per_step.get)
             if plan.n_stages > 1:
                 model.set_serial_steps(True)
@@ -443,10 +447,11 @@ def main():
     n = world
     tok_s = job_rate(n, B, K, elapsed_ms / 1e3)
     if M:
-        # weights once per step; each verify row reads its own rows [0, pos + j]
+        # weights once per step; the one chunk-attention launch per layer reads the
+        # sequence's rows [0, pos + M) once for all M rows; M rows written, M logits
         one = cfg.replace(batch=1)
-        step_bytes = [one.step_bytes(ctx + i * M) + sum(one.step_bytes(ctx + i * M + j) - one.weight_bytes()
-                                                         for j in range(1, M)) for i in range(K)]
+        row = cfg.n_layers * 2 * cfg.kv_heads * cfg.head_dim * 2
+        step_bytes = [one.step_bytes(ctx + i * M + M - 1) + (M - 1) * (row + cfg.vocab * 4) for i in range(K)]
     else:
         step_bytes = [cfg.step_bytes(ctx + i) for i in range(K)]
     hbm_gbs = sum(step_bytes) / (elapsed_ms / 1e3) / 1e9

@@ -214,6 +214,7 @@ struct ChunkAttnParams {
   CUtensorMap tmap_v;
   const float* q;              // [ntok][nq*hd]
   float* part;                 // [ntok][nq][max_chunks][hd + 4]: o, m, l
+  float* out;                  // when set: the merged o as fp32 [ntok][nq*hd] instead of the planes
   __nv_bfloat16* xo;
   int nq, nkv, hd, max_ctx, max_chunks;
   int chunk, nchunks;          // keys per CTA, CTAs per (block, kv head): chunk_attn_split

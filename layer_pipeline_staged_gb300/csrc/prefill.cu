@@ -343,7 +343,8 @@ __global__ void __launch_bounds__(256) chunk_attn_kernel(const __grid_constant__
 }
 
 // Token j: combine its key chunks in chunk order and write the o-projection's
-// activation planes xo[j] = bf16(o), xo[NP + j] = bf16(o - bf16(o)). Warp w
+// activation planes xo[j] = bf16(o), xo[NP + j] = bf16(o - bf16(o)) (or, with
+// `out` set, o itself as fp32). Warp w
 // takes heads w, w + 8, ...: the chunks' weights exp(m_c - M) once per head
 // (lane c, c + 32, ...; then fixed warp trees), then every dimension's sum
 // over the chunks in chunk order.
@@ -375,10 +376,14 @@ __global__ void __launch_bounds__(256) chunk_merge_kernel(const __grid_constant_
       float O = 0.f;
       for (int c = 0; c < nch; ++c) O += base[c * (HD + 4) + d] * wsm[warp][c];
       const float o = O / L;
-      const __nv_bfloat16 hi = __float2bfloat16_rn(o);
       const size_t idx = static_cast<size_t>(h) * HD + d;
-      p.xo[static_cast<size_t>(j) * qw + idx] = hi;
-      p.xo[static_cast<size_t>(p.NP + j) * qw + idx] = __float2bfloat16_rn(o - __bfloat162float(hi));
+      if (p.out) {
+        p.out[static_cast<size_t>(j) * qw + idx] = o;
+      } else {
+        const __nv_bfloat16 hi = __float2bfloat16_rn(o);
+        p.xo[static_cast<size_t>(j) * qw + idx] = hi;
+        p.xo[static_cast<size_t>(p.NP + j) * qw + idx] = __float2bfloat16_rn(o - __bfloat162float(hi));
+      }
     }
     __syncwarp();
   }

@@ -717,7 +717,7 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
   }
 
   // chunking of the attention partials, sized for the longest context (the
-  // verify arm attends one row per launch)
+  // verify arm runs the causal chunk attention instead)
   m->verify = (d.flags & LPS_FLAG_VERIFY) != 0;
   m->attn_max_chunks = attn_max_chunks(hd, nkv, m->verify ? 1 : B, d.max_ctx, m->num_sms);
   // batch 1, on request: the persistent stage kernel where its shapes fit
@@ -762,7 +762,9 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
     S.q = static_cast<float*>(dev_alloc(m, sizeof(float) * B * qw));
     S.o = static_cast<float*>(dev_alloc(m, sizeof(float) * B * qw));
     S.a = static_cast<float*>(dev_alloc(m, sizeof(float) * B * d.ffn));
-    const size_t part_chunks = m->persist ? static_cast<size_t>(m->skp.nch_max) : static_cast<size_t>(m->attn_max_chunks);
+    const size_t part_chunks = m->persist  ? static_cast<size_t>(m->skp.nch_max)
+                               : m->verify ? static_cast<size_t>(chunk_attn_max_chunks(nkv, m->num_sms))
+                                           : static_cast<size_t>(m->attn_max_chunks);
     S.part = static_cast<float*>(dev_alloc(m, sizeof(float) * B * nq * part_chunks * (hd + 4)));
     S.counter = static_cast<int*>(dev_alloc(m, sizeof(int) * B * nkv));
     S.rope = static_cast<float2*>(dev_alloc(m, sizeof(float2) * rope.size()));
@@ -1236,18 +1238,31 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
         if (!m->verify) {
           LAUNCH(LPS_KERNEL_ATTN, cs, ap, launch_attention(ap, B, max_pos, cs, pdl));
         } else {
-          // verify rows share the one cache: one launch per row b, attending
-          // [0, pos[b]] (rows pos[0]..pos[b] were written by this step's QKV)
-          for (int b = 0; b < B; ++b) {
-            AttnParams ab = ap;
-            ab.q = S.q + static_cast<size_t>(b) * qw;
-            ab.out = o_buf + static_cast<size_t>(b) * qw;
-            ab.part = S.part + static_cast<size_t>(b) * nq * m->attn_max_chunks * (hd + 4);
-            ab.counter = S.counter + static_cast<size_t>(b) * nkv;
-            ab.pos[0] = pos[b];
-            ab.chunk = attn_chunk(hd, nkv, 1, pos[b], m->num_sms);
-            LAUNCH(LPS_KERNEL_ATTN, cs, ab, launch_attention(ab, 1, pos[b], cs, pdl));
-          }
+          // verify rows share the one cache: row b (position pos[0] + b) attends
+          // [0, pos[0] + b], rows pos[0].. written by this step's QKV: one
+          // causal chunk-attention launch (and its merge) for all rows
+          ChunkAttnParams cp{};
+          cp.tmap_k = L.tmap_k;
+          cp.tmap_v = L.tmap_v;
+          cp.q = S.q;
+          cp.part = S.part;
+          cp.out = o_buf;
+          cp.nq = nq;
+          cp.nkv = nkv;
+          cp.hd = hd;
+          cp.max_ctx = d.max_ctx;
+          cp.max_chunks = chunk_attn_max_chunks(nkv, m->num_sms);
+          chunk_attn_split(hd, nkv, B, pos[0], m->num_sms, &cp.nchunks, &cp.chunk);
+          cp.seq = 0;
+          cp.pos0 = pos[0];
+          cp.ntok = B;
+          cp.NP = B;
+          cp.scale = ap.scale;
+          cp.wait_limit = m->wait_limit;
+          cp.status = m->status_dev;
+          cp.trace_merge = nullptr;
+          LAUNCH(LPS_KERNEL_ATTN, cs, cp, launch_chunk_attn(cp, cs, pdl));
+          ++launches;  // the merge
         }
       }
       // o-proj + residual (the first layer of a later stage reads the boundary slot)
