@@ -496,28 +496,40 @@ cudaError_t launch_h(const AttnParams& p, int batch, int max_pos, cudaStream_t s
 int attn_sub_tile(int hd) { return 8192 / hd; }
 
 // Positions per CTA: a whole number cs of sub-tiles, chosen for the shortest
-// modelled time: waves of two resident CTAs per SM, each wave as long as cs
-// sub-tiles plus a fixed per-CTA cost (start-up, first copy, partial write)
-// of about two sub-tiles; ties go to the longer chunk (fewer partials to
-// combine). Every CTA of a wave streams at about the same rate, so the cached
-// bytes spread evenly over the SMs without a ragged last wave.
-int attn_chunk(int hd, int nkv, int batch, int max_pos, int num_sms) {
+// modelled time, with `slots` CTAs per SM sharing the SM's share of HBM: the
+// busiest SM takes ceil(CTAs / (slots x SMs)) rounds of cs sub-tiles plus a
+// fixed per-CTA cost (start-up, first copy, partial write) of about two
+// sub-tiles; ties go to the longer chunk (fewer partials to combine).
+static int attn_chunk_model(int nsub, long long groups, int num_sms, int slots) {
   constexpr long long kOverhead = 2;
-  const int ts = attn_sub_tile(hd);
-  const int nsub = (max_pos + 1 + ts - 1) / ts;  // sub-tiles of one (sequence, kv head)
-  const long long groups = static_cast<long long>(nkv) * batch;
-  const long long slots = 2LL * num_sms;
   long long best = -1;
   int best_cs = nsub;
   for (int cs = 1; cs <= nsub; ++cs) {
     const long long ctas = groups * ((nsub + cs - 1) / cs);
-    const long long cost = (ctas + slots - 1) / slots * (cs + kOverhead);
+    const long long per = static_cast<long long>(slots) * num_sms;
+    const long long cost = (ctas + per - 1) / per * (cs + kOverhead);
     if (best < 0 || cost <= best) {
       best = cost;
       best_cs = cs;
     }
   }
-  return best_cs * ts;
+  return best_cs;
+}
+
+// Balancing the bytes per SM (one CTA slot per SM in the model) gives fewer
+// partials to merge and measured faster, except where it leaves one CTA per
+// SM with a long chunk: its four warps are then latency-bound, and two
+// resident CTAs per SM with half the chunk measured faster (8B shapes: one
+// slot wins at context 8192 batch 1 and at context 4096 batch 4, two slots
+// at context 32768 batch 1).
+int attn_chunk(int hd, int nkv, int batch, int max_pos, int num_sms) {
+  const int ts = attn_sub_tile(hd);
+  const int nsub = (max_pos + 1 + ts - 1) / ts;  // sub-tiles of one (sequence, kv head)
+  const long long groups = static_cast<long long>(nkv) * batch;
+  const int cs1 = attn_chunk_model(nsub, groups, num_sms, 1);
+  const long long ctas1 = groups * ((nsub + cs1 - 1) / cs1);
+  if (cs1 <= 24 || ctas1 > num_sms) return cs1 * ts;
+  return attn_chunk_model(nsub, groups, num_sms, 2) * ts;
 }
 
 int attn_max_chunks(int hd, int nkv, int batch, int max_ctx, int num_sms) {
