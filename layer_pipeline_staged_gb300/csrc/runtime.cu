@@ -180,6 +180,9 @@ struct LayerDev {
   __nv_bfloat16* vc = nullptr;
   float* o_keep = nullptr;      // [B][nq*hd] with LPS_FLAG_KEEP_ATTN_OUT
   CUtensorMap tmap_k{}, tmap_v{};  // the caches as 2D TMA tensors (attention sub-tile boxes)
+  // bf16 weights in the row-major layout as 2D TMA tensors (64 x 128 boxes,
+  // 128-byte swizzle) for the prefill's tensor-core GEMMs
+  CUtensorMap tm_qkv{}, tm_o{}, tm_gu{}, tm_d{};
 };
 
 struct StageDev {
@@ -226,7 +229,6 @@ struct PrefillStage {
   int* gcnt = nullptr;              // GEMM tile counters (zero between launches)
   int32_t* tok = nullptr;           // stage 0: the prompt's token ids [max_ctx]
   CUtensorMap map_x{}, map_xo{}, map_xd{};
-  std::vector<CUtensorMap> map_qkv, map_o, map_gu, map_d;  // per layer of the stage
 };
 struct PrefillState {
   bool ready = false;
@@ -654,7 +656,6 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
   m->int8 = int8;
   m->single = (d.flags & LPS_FLAG_SINGLE_STREAM) != 0;
   m->overlap = (d.flags & LPS_FLAG_SERIAL_STEPS) == 0;
-  m->skinny = d.batch > 1;
   m->fence = plan->fence;
   m->N = static_cast<int>(plan->fence.size()) - 1;
   m->device = rt ? rt->device : 0;
@@ -690,6 +691,7 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
   if (e != cudaSuccess) return bail(LPS_ECUDA, std::string("cudaSetDevice: ") + cudaGetErrorString(e));
   if (cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) != cudaSuccess)
     return bail(LPS_ECUDA, "cudaDeviceGetAttribute failed");
+  m->skinny = d.batch > 1;
 
   const int N = m->N, B = d.batch, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads, E = d.n_embd;
   const int half = hd / 2;
@@ -841,6 +843,11 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
               m, up, E, d.ffn, [&](int r) { return static_cast<const char*>(L.w_down.w) + rbF * r; },
               [&](int r) { return L.w_down.scale[r]; }, &D.w_d, &D.s_d, &S.sk_d, temp, &why))
         return bail(LPS_ENOMEM, "W_down upload: " + why);
+      // the row-major bf16 weights as TMA tensors for the tensor-core GEMMs
+      if (!m->skinny && !int8 &&
+          !(make_bf16_map(&D.tm_qkv, D.w_qkv, E, rows_qkv, 128) && make_bf16_map(&D.tm_o, D.w_o, qw, E, 128) &&
+            make_bf16_map(&D.tm_gu, D.w_gu, E, 2 * d.ffn, 128) && make_bf16_map(&D.tm_d, D.w_d, d.ffn, E, 128)))
+        return bail(LPS_ECUDA, "cuTensorMapEncodeTiled failed for a weight matrix");
       D.attn_norm = static_cast<float*>(dev_alloc(m, sizeof(float) * E));
       D.ffn_norm = static_cast<float*>(dev_alloc(m, sizeof(float) * E));
       D.kc = static_cast<__nv_bfloat16*>(dev_alloc(m, kv_elems * 2));
@@ -1442,16 +1449,6 @@ int prefill_init(lps_model* m, const char* FN) {
     CK(cudaMemsetAsync(F.xd, 0, sizeof(__nv_bfloat16) * 2 * NP * ffn, S.stream), "cudaMemsetAsync");
     bool ok = make_bf16_map(&F.map_x, F.x, E, 2 * NP, NP) && make_bf16_map(&F.map_xo, F.xo, qw, 2 * NP, NP) &&
               make_bf16_map(&F.map_xd, F.xd, ffn, 2 * NP, NP);
-    const size_t nl = S.layers.size();
-    F.map_qkv.resize(nl);
-    F.map_o.resize(nl);
-    F.map_gu.resize(nl);
-    F.map_d.resize(nl);
-    for (size_t i = 0; i < nl && ok; ++i) {
-      const LayerDev& L = S.layers[i];
-      ok = make_bf16_map(&F.map_qkv[i], L.w_qkv, E, rows_qkv, 128) && make_bf16_map(&F.map_o[i], L.w_o, qw, E, 128) &&
-           make_bf16_map(&F.map_gu[i], L.w_gu, E, 2 * ffn, 128) && make_bf16_map(&F.map_d[i], L.w_d, ffn, E, 128);
-    }
     if (!ok) return fail(LPS_ECUDA, FN, "cuTensorMapEncodeTiled failed for a prefill operand");
   }
   P.bd.assign(N > 1 ? N - 1 : 0, Boundary{});
@@ -1547,7 +1544,7 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
       pp.gain = L.attn_norm;
       PF_LAUNCH(launch_prep(pp, cs, pdl));
       TcGemmParams gq = g;
-      gq.tmap_w = F.map_qkv[i];
+      gq.tmap_w = L.tm_qkv;
       gq.tmap_x = F.map_x;
       gq.R = (nq + 2 * nkv) * hd;
       gq.K = E;
@@ -1581,7 +1578,7 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
       ++launches;  // the merge
       // o-proj + residual
       TcGemmParams go = g;
-      go.tmap_w = F.map_o[i];
+      go.tmap_w = L.tm_o;
       go.tmap_x = F.map_xo;
       go.R = E;
       go.K = qw;
@@ -1591,7 +1588,7 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
       pp.gain = L.ffn_norm;
       PF_LAUNCH(launch_prep(pp, cs, pdl));
       TcGemmParams gg = g;
-      gg.tmap_w = F.map_gu[i];
+      gg.tmap_w = L.tm_gu;
       gg.tmap_x = F.map_x;
       gg.R = 2 * ffn;
       gg.K = E;
@@ -1601,7 +1598,7 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
       PF_LAUNCH(launch_tc_gemm(gg, P.plan, cs, pdl));
       // down + residual
       TcGemmParams gd = g;
-      gd.tmap_w = F.map_d[i];
+      gd.tmap_w = L.tm_d;
       gd.tmap_x = F.map_xd;
       gd.R = E;
       gd.K = ffn;
@@ -1764,9 +1761,10 @@ extern "C" int model_prefill(lps_model* m, int b, const int32_t* tokens, int n, 
   if (!m) return fail(LPS_EINVAL, FN, "model is NULL");
   if (m->failed) return fail(LPS_ECUDA, FN, "model is in a failed state after an earlier device error");
   const lps_model_desc& d = m->d;
-  if (m->skinny || m->verify)
-    return fail(LPS_EINVAL, FN, "prefill needs the row-major weight layout of a batch-1 model");
   if (m->int8) return fail(LPS_EINVAL, FN, "prefill needs bf16 weights");
+  if (m->skinny || m->verify)
+    return fail(LPS_EINVAL, FN, "prefill needs the row-major weight layout of a batch-1 model (not batch > 1, "
+                                "not verify rows)");
   if (!tokens || n < 1) return fail(LPS_EINVAL, FN, "tokens is NULL or n < 1");
   if (b < 0 || b >= static_cast<int>(m->filled.size())) return fail(LPS_EINVAL, FN, "sequence out of range");
   if (pos0 < 0 || pos0 > m->filled[b]) return fail(LPS_EINVAL, FN, "pos0 skips unwritten cache rows (pos0 > filled)");

@@ -186,8 +186,12 @@ def test_prefill_argument_checks(tiny):
     with pytest.raises(lps.LpsError) as ei:
         mq.prefill(toks[:4])
     assert ei.value.code == lps.LPS_EINVAL and "bf16" in str(ei.value)
+    vm = bind(TINY.replace(name="tiny_v2", batch=2), w, max_ctx=16, flags=lps.LPS_FLAG_VERIFY)
+    with pytest.raises(lps.LpsError) as ei:
+        vm.prefill(toks[:4])
+    assert ei.value.code == lps.LPS_EINVAL and "verify" in str(ei.value)
     b2 = TINY.replace(name="tiny_b2", batch=2)
     mb = bind(b2, synth.make_weights(b2), max_ctx=16)
     with pytest.raises(lps.LpsError) as ei:
         mb.prefill(toks[:4])
-    assert ei.value.code == lps.LPS_EINVAL and "batch-1" in str(ei.value)
+    assert ei.value.code == lps.LPS_EINVAL and "row-major" in str(ei.value)
