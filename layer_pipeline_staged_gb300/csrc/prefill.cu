@@ -34,8 +34,16 @@ constexpr int kMaxMergeChunks = 320;  // key chunks per token the merge takes (c
 
 // ---- activation planes --------------------------------------------------------
 
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
 // Row j < ntok: x = src[j] (K floats), optionally RMS-normalised with `gain`;
 // X[j] = bf16(x), X[NP + j] = bf16(x - bf16(x)). Rows [ntok, NP) become zero.
+// Each thread loads its float4 groups of the row (and of the gain) into
+// registers at once, up to kPrepVec of them; longer rows loop.
+constexpr int kPrepVec = 8;
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const __grid_constant__ PrepParams p) {
   __shared__ float red[kPrepThreads / 32];
   __shared__ float s_inv;
@@ -44,22 +52,38 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const __grid_constan
   const int j = blockIdx.x, tid = threadIdx.x;
   __nv_bfloat16* hi = p.x + static_cast<size_t>(j) * p.K;
   __nv_bfloat16* lo = p.x + static_cast<size_t>(p.NP + j) * p.K;
+  const int K4 = p.K / 4;
   pdl_wait();
   if (j >= p.ntok) {
-    const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
-    for (int k = tid; k < p.K; k += kPrepThreads) {
-      hi[k] = z;
-      lo[k] = z;
+    for (int k = tid; k < K4; k += kPrepThreads) {
+      reinterpret_cast<uint2*>(hi)[k] = make_uint2(0, 0);
+      reinterpret_cast<uint2*>(lo)[k] = make_uint2(0, 0);
     }
     trace_end(p.trace);
     return;
   }
-  const float* src = p.src + static_cast<size_t>(j) * p.lds;
+  const float4* src = reinterpret_cast<const float4*>(p.src + static_cast<size_t>(j) * p.lds);
+  const float4* g4 = reinterpret_cast<const float4*>(p.gain);
   float inv = 1.f;
   if (p.gain) {
-    // mean square: thread t sums k = t, t + 256, ...; then the warps' sums in warp order
+    // mean square: thread t sums the groups t, t + 256, ... in order; then the
+    // warps' sums in warp order
     float ss = 0.f;
-    for (int k = tid; k < p.K; k += kPrepThreads) ss = fmaf(src[k], src[k], ss);
+    for (int k0 = tid; k0 < K4; k0 += kPrepVec * kPrepThreads) {
+      float4 v[kPrepVec];
+#pragma unroll
+      for (int u = 0; u < kPrepVec; ++u) {
+        const int k = k0 + u * kPrepThreads;
+        v[u] = k < K4 ? src[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kPrepVec; ++u) {
+        ss = fmaf(v[u].x, v[u].x, ss);
+        ss = fmaf(v[u].y, v[u].y, ss);
+        ss = fmaf(v[u].z, v[u].z, ss);
+        ss = fmaf(v[u].w, v[u].w, ss);
+      }
+    }
     ss = warp_sum(ss);
     if ((tid & 31) == 0) red[tid >> 5] = ss;
     __syncthreads();
@@ -71,11 +95,28 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const __grid_constan
     __syncthreads();
     inv = s_inv;
   }
-  for (int k = tid; k < p.K; k += kPrepThreads) {
-    const float v = p.gain ? src[k] * inv * p.gain[k] : src[k];
-    const __nv_bfloat16 h = __float2bfloat16_rn(v);
-    hi[k] = h;
-    lo[k] = __float2bfloat16_rn(v - __bfloat162float(h));
+  for (int k0 = tid; k0 < K4; k0 += kPrepVec * kPrepThreads) {
+    float4 v[kPrepVec], g[kPrepVec];
+#pragma unroll
+    for (int u = 0; u < kPrepVec; ++u) {
+      const int k = k0 + u * kPrepThreads;
+      v[u] = k < K4 ? src[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+      g[u] = (p.gain && k < K4) ? __ldg(g4 + k) : make_float4(1.f, 1.f, 1.f, 1.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kPrepVec; ++u) {
+      const int k = k0 + u * kPrepThreads;
+      if (k >= K4) break;
+      const float x[4] = {v[u].x * inv * g[u].x, v[u].y * inv * g[u].y, v[u].z * inv * g[u].z, v[u].w * inv * g[u].w};
+      float h[4], l[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        h[e] = __bfloat162float(__float2bfloat16_rn(x[e]));
+        l[e] = x[e] - h[e];
+      }
+      reinterpret_cast<uint2*>(hi)[k] = make_uint2(pack_bf16(h[0], h[1]), pack_bf16(h[2], h[3]));
+      reinterpret_cast<uint2*>(lo)[k] = make_uint2(pack_bf16(l[0], l[1]), pack_bf16(l[2], l[3]));
+    }
   }
   trace_end(p.trace);
 }
@@ -126,10 +167,6 @@ __device__ __forceinline__ void mma_add(float* c, const uint32_t* a, uint32_t b0
   c[1] += d1;
   c[2] += d2;
   c[3] += d3;
-}
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
 }
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 // Byte offset of 16-byte chunk c of row r inside a 128-byte-swizzled box.
@@ -342,23 +379,24 @@ __global__ void __launch_bounds__(256) chunk_attn_kernel(const __grid_constant__
   trace_end(p.trace);
 }
 
-// Token j: combine its key chunks in chunk order and write the o-projection's
-// activation planes xo[j] = bf16(o), xo[NP + j] = bf16(o - bf16(o)) (or, with
-// `out` set, o itself as fp32). Warp w
-// takes heads w, w + 8, ...: the chunks' weights exp(m_c - M) once per head
-// (lane c, c + 32, ...; then fixed warp trees), then every dimension's sum
-// over the chunks in chunk order.
+// One warp per (token j, head h): combine the key chunks of the pair in chunk
+// order and write the o-projection's activation planes xo[j] = bf16(o),
+// xo[NP + j] = bf16(o - bf16(o)) (or, with `out` set, o itself as fp32). The
+// chunk weights exp(m_c - M) are formed once (lane c, c + 32, ...; then fixed
+// warp trees), then every dimension's sum over the chunks in chunk order.
 template <int HD>
 __global__ void __launch_bounds__(256) chunk_merge_kernel(const __grid_constant__ ChunkAttnParams p) {
   __shared__ float wsm[8][kMaxMergeChunks];
   trace_start(p.trace);
   pdl_launch_dependents();
   pdl_wait();
-  const int j = blockIdx.x, qw = p.nq * HD, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int j0 = (j / 16) * 16, jn = min(16, p.ntok - j0);
-  const int kend = p.pos0 + j0 + jn;
-  const int nch = (kend + p.chunk - 1) / p.chunk;
-  for (int h = warp; h < p.nq; h += 8) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pair = blockIdx.x * 8 + warp;
+  if (pair < p.ntok * p.nq) {
+    const int j = pair / p.nq, h = pair - j * p.nq, qw = p.nq * HD;
+    const int j0 = (j / 16) * 16, jn = min(16, p.ntok - j0);
+    const int kend = p.pos0 + j0 + jn;
+    const int nch = (kend + p.chunk - 1) / p.chunk;
     const float* base = p.part + (static_cast<size_t>(j) * p.nq + h) * p.max_chunks * (HD + 4);
     float mloc = -INFINITY;
     for (int c = lane; c < nch; c += 32) mloc = fmaxf(mloc, base[c * (HD + 4) + HD]);
@@ -372,11 +410,22 @@ __global__ void __launch_bounds__(256) chunk_merge_kernel(const __grid_constant_
     }
     const float L = warp_sum(lloc);
     __syncwarp();
-    for (int d = lane; d < HD; d += 32) {
-      float O = 0.f;
-      for (int c = 0; c < nch; ++c) O += base[c * (HD + 4) + d] * wsm[warp][c];
-      const float o = O / L;
-      const size_t idx = static_cast<size_t>(h) * HD + d;
+    constexpr int PER = HD / 32;  // dimensions per lane
+    float O[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) O[e] = 0.f;
+    for (int c = 0; c < nch; ++c) {
+      const float wc = wsm[warp][c];
+      float t[PER];
+#pragma unroll
+      for (int e = 0; e < PER; ++e) t[e] = base[c * (HD + 4) + lane + 32 * e];
+#pragma unroll
+      for (int e = 0; e < PER; ++e) O[e] += t[e] * wc;
+    }
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      const float o = O[e] / L;
+      const size_t idx = static_cast<size_t>(h) * HD + lane + 32 * e;
       if (p.out) {
         p.out[static_cast<size_t>(j) * qw + idx] = o;
       } else {
@@ -385,7 +434,6 @@ __global__ void __launch_bounds__(256) chunk_merge_kernel(const __grid_constant_
         p.xo[static_cast<size_t>(p.NP + j) * qw + idx] = __float2bfloat16_rn(o - __bfloat162float(hi));
       }
     }
-    __syncwarp();
   }
   trace_end(p.trace);
 }
@@ -418,7 +466,7 @@ cudaError_t launch_chunk_attn_t(const ChunkAttnParams& p, cudaStream_t s, bool p
   if (e != cudaSuccess) return e;
   ChunkAttnParams q = p;
   q.trace = p.trace_merge;
-  return launch_ex(chunk_merge_kernel<HD>, q, dim3(p.ntok), dim3(256), 0, s, true);
+  return launch_ex(chunk_merge_kernel<HD>, q, dim3((p.ntok * p.nq + 7) / 8), dim3(256), 0, s, true);
 }
 
 }  // namespace
