@@ -7,7 +7,8 @@
 - full contexts (8B at 8192 with 4 stages and deferred readback, 8B-q8 at
   32768 with batch 1 and 8): a state transplant -- the same cache rows are
   imported into both sides -- then decode steps in the launch configuration
-  the benchmark times, compared at every sequence.
+  the benchmark times, compared at every sequence; for the 8B bf16 context the
+  rows are also written by the kernels' own chunked prefill of the prompt.
 """
 import numpy as np
 import pytest
@@ -109,6 +110,35 @@ def test_1b_whole_sequence():
     assert np.array_equal(np.stack([m1.decode_step(toks[t], t) for t in range(T)]), got)
     st = m4.stats()
     assert st["boundary_crossings"] == 3 * T and st["deferred_steps"] == T
+
+
+def test_8b_full_context_from_prefill():
+    """The 8B bf16 workload's full context written by the kernels themselves:
+    its 8192-token seeded prompt prefilled in chunks of 128 through the 4
+    stages (cuts 8/16/24) and through 1 stage, bit-identical (logits and cache
+    rows); then the oracle, given the prefilled cache rows, on two decode steps
+    after them (realistic cache magnitudes, not uniform synthetic rows), and
+    bit-identity of four deferred steps with one stage and with eager readback."""
+    cfg = synth.CONFIGS["8b"]
+    P, T = cfg.ctx, 4
+    max_ctx = P + T
+    w = synth.make_weights(cfg)
+    prompt = synth.make_tokens(cfg, P, seed=cfg.seed_t + 9)
+    m = bind(cfg, w, max_ctx=max_ctx, pending_depth=4)
+    m1 = bind(cfg, w, max_ctx=max_ctx, fence=(0, cfg.n_layers))
+    lg, lg1 = m.prefill(prompt), m1.prefill(prompt)
+    assert np.array_equal(lg, lg1)
+    orc = oracle.Oracle(cfg, w, max_ctx=max_ctx)
+    for l in range(cfg.n_layers):
+        k, v = m.kv_export(l, 0)
+        k1, v1 = m1.kv_export(l, 0)
+        assert np.array_equal(k, k1) and np.array_equal(v, v1), l
+        orc.kv_import(l, 0, k, v, P)
+    toks = synth.make_tokens(cfg, T, seed=cfg.seed_t + 5)
+    got = _deferred_steps(m, toks, P)
+    for t in range(2):
+        assert_close(got[t], orc.step(toks[t], P + t), cfg, f"8b step {t} after the prefilled context")
+    _bitwise_arms(cfg, w, m, m1, toks, P, got)
 
 
 @pytest.mark.parametrize("name", ["8b", "8b_q8", "8b_q8_b8"])
