@@ -10,8 +10,8 @@ heads, head_dim 128, ffn 14336, vocab 128256), bf16 weights and KV cache,
 batch 1, 4 stages (cuts 8, 16, 24), context 8192, 256 decode steps, deferred
 logits readback. Weights are seeded N(0, 0.02) (synthetic: no checkpoint);
 the context's cache rows are written by the chunked prefill of a seeded prompt
-(model_prefill, timed and reported as "prefill"; int8 and batch > 1 workloads
-fill them synthetically, as their values do not change the step time); the weights (15 GB) are far larger than L2, so every step streams
+(model_prefill, timed and reported as "prefill"; batch > 1 workloads fill them
+synthetically, as their values do not change the step time); the weights (15 GB) are far larger than L2, so every step streams
 them from HBM.
 
 Prints one JSON line. ``--impl reference`` times the CPU oracle on the same
@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--fill", default="auto", choices=["auto", "prefill", "synthetic", "decode"],
                     help="how the context rows before the timed steps are written: model_prefill (chunked "
                          "prefill through the stages, timed and reported), synthetic rows, or decode steps; "
-                         "auto = prefill where the model takes it (batch 1, bf16 weights), else synthetic")
+                         "auto = prefill where the model takes it (batch 1), else synthetic")
     ap.add_argument("--serial", action="store_true", help="no overlap between consecutive steps' stages")
     ap.add_argument("--stages", type=int, default=0,
                     help="even split into this many stages instead of the workload's own cuts (0 = the workload's)")
@@ -311,7 +311,7 @@ def main():
     # cache contents, or teacher-forced decode steps
     fill = args.fill
     if fill == "auto":
-        fill = "prefill" if (B == 1 and not M and cfg.weight_dtype == "bf16") else "synthetic"
+        fill = "prefill" if (B == 1 and not M) else "synthetic"
     prefill_info = None
     if fill == "prefill" and start > 0:
         ptoks = synth.make_tokens(cfg, start, seed=cfg.seed_t + 9)

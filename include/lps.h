@@ -266,7 +266,8 @@ int decode_step_device(lps_model* m, const int32_t* tokens, const int32_t* pos, 
  * of every layer; afterwards filled[b] = max(filled[b], pos0 + n), and decode
  * continues at pos0 + n. logits (host float[vocab], may be NULL) receives the
  * last prompt token's logits. Returns once the prefill has completed.
- * Requires a batch-1 model with bf16 weights (the row-major weight layout),
+ * Requires a batch-1 model (the row-major weight layout; bf16 weights, or int8
+ * ones widened to bf16 in shared memory with the row scale on the result),
  * 0 <= pos0 <= filled[b], pos0 + n <= max_ctx and 0 <= tokens[i] < vocab;
  * else LPS_EINVAL. The first call allocates the prefill buffers (through the
  * model's allocator; LPS_ENOMEM on failure). Results match the oracle within

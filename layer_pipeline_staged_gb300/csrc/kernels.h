@@ -160,7 +160,9 @@ cudaError_t launch_attention(const AttnParams& p, int batch, int max_pos, cudaSt
 // kEpiResidual (h[j][r] += y), kEpiSwiglu (a = silu(gate) * up written as the
 // down projection's two bf16 planes xo [2][NP][ldx]).
 struct TcGemmParams {
-  CUtensorMap tmap_w;          // W [R][K] bf16: box 64 x 128, 128-byte swizzle
+  CUtensorMap tmap_w;          // W [R][K]: bf16 (box 64 x 128, 128-byte swizzle) or int8 (box 64 x 128, unswizzled)
+  const float* wscale;         // int8: per packed row scale; else nullptr
+  int int8;                    // 1: int8 weights, widened to bf16 in shared memory
   CUtensorMap tmap_x;          // X [2*NP][K] bf16: box 64 x NP, 128-byte swizzle
   int R, K, NP, ntok, epi;
   int stages, tmem_cols;       // set from the plan at launch
@@ -185,12 +187,15 @@ struct TcGemmPlan {
   bool ok;
 };
 constexpr int kTcMaxTokens = 128;  // token rows of one prefill chunk (NP <= 128)
-TcGemmPlan tc_gemm_plan(int NP, int num_sms, int max_smem);
+TcGemmPlan tc_gemm_plan(int NP, bool int8, int num_sms, int max_smem);
 int tc_gemm_tiles(int R);
 cudaError_t launch_tc_gemm(const TcGemmParams& p, const TcGemmPlan& plan, cudaStream_t s, bool pdl);
 // 2D bf16 tensor map over a row-major [rows][cols] matrix with boxes of 64
 // columns x box_rows rows and the 128-byte swizzle.
 bool make_bf16_map(CUtensorMap* map, const void* base, unsigned long long cols, unsigned long long rows, int box_rows);
+// The same for a row-major int8 matrix, boxes of 64 columns (bytes) x box_rows
+// rows without a swizzle.
+bool make_i8_map(CUtensorMap* map, const void* base, unsigned long long cols, unsigned long long rows, int box_rows);
 
 // ---- prefill chunk: activation planes and chunk attention ------------------------
 // Rows j < ntok of src [ntok][lds] (RMS-normalised with gain when gain != null)

@@ -180,8 +180,8 @@ struct LayerDev {
   __nv_bfloat16* vc = nullptr;
   float* o_keep = nullptr;      // [B][nq*hd] with LPS_FLAG_KEEP_ATTN_OUT
   CUtensorMap tmap_k{}, tmap_v{};  // the caches as 2D TMA tensors (attention sub-tile boxes)
-  // bf16 weights in the row-major layout as 2D TMA tensors (64 x 128 boxes,
-  // 128-byte swizzle) for the prefill's tensor-core GEMMs
+  // the weights in the row-major layout as 2D TMA tensors (64 x 128 boxes;
+  // bf16 with the 128-byte swizzle, int8 unswizzled) for the prefill's GEMMs
   CUtensorMap tm_qkv{}, tm_o{}, tm_gu{}, tm_d{};
 };
 
@@ -543,6 +543,17 @@ bool make_bf16_map(CUtensorMap* map, const void* base, unsigned long long cols, 
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+bool make_i8_map(CUtensorMap* map, const void* base, unsigned long long cols, unsigned long long rows, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), rows};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 }  // namespace lps
 
 namespace {
@@ -843,11 +854,13 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
               m, up, E, d.ffn, [&](int r) { return static_cast<const char*>(L.w_down.w) + rbF * r; },
               [&](int r) { return L.w_down.scale[r]; }, &D.w_d, &D.s_d, &S.sk_d, temp, &why))
         return bail(LPS_ENOMEM, "W_down upload: " + why);
-      // the row-major bf16 weights as TMA tensors for the tensor-core GEMMs
-      if (!m->skinny && !int8 &&
-          !(make_bf16_map(&D.tm_qkv, D.w_qkv, E, rows_qkv, 128) && make_bf16_map(&D.tm_o, D.w_o, qw, E, 128) &&
-            make_bf16_map(&D.tm_gu, D.w_gu, E, 2 * d.ffn, 128) && make_bf16_map(&D.tm_d, D.w_d, d.ffn, E, 128)))
-        return bail(LPS_ECUDA, "cuTensorMapEncodeTiled failed for a weight matrix");
+      // the row-major weights as TMA tensors for the prefill's tensor-core GEMMs
+      if (!m->skinny) {
+        auto mk = int8 ? make_i8_map : make_bf16_map;
+        if (!(mk(&D.tm_qkv, D.w_qkv, E, rows_qkv, 128) && mk(&D.tm_o, D.w_o, qw, E, 128) &&
+              mk(&D.tm_gu, D.w_gu, E, 2 * d.ffn, 128) && mk(&D.tm_d, D.w_d, d.ffn, E, 128)))
+          return bail(LPS_ECUDA, "cuTensorMapEncodeTiled failed for a weight matrix");
+      }
       D.attn_norm = static_cast<float*>(dev_alloc(m, sizeof(float) * E));
       D.ffn_norm = static_cast<float*>(dev_alloc(m, sizeof(float) * E));
       D.kc = static_cast<__nv_bfloat16*>(dev_alloc(m, kv_elems * 2));
@@ -1422,7 +1435,7 @@ int prefill_init(lps_model* m, const char* FN) {
   int max_smem = 0;
   CK(cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, m->device), "device attribute");
   const int C = kTcMaxTokens, NP = kTcMaxTokens;
-  P.plan = tc_gemm_plan(NP, m->num_sms, max_smem);
+  P.plan = tc_gemm_plan(NP, m->int8, m->num_sms, max_smem);
   if (!P.plan.ok) return fail(LPS_EINVAL, FN, "the prefill GEMM does not fit this device");
   P.C = C;
   P.NP = NP;
@@ -1529,6 +1542,7 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
     g.counter = F.gcnt;
     g.wait_limit = m->wait_limit;
     g.status = m->status_dev;
+    g.int8 = m->int8 ? 1 : 0;
     PrepParams pp{};
     pp.src = F.h;
     pp.lds = E;
@@ -1545,6 +1559,7 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
       PF_LAUNCH(launch_prep(pp, cs, pdl));
       TcGemmParams gq = g;
       gq.tmap_w = L.tm_qkv;
+      gq.wscale = L.s_qkv;
       gq.tmap_x = F.map_x;
       gq.R = (nq + 2 * nkv) * hd;
       gq.K = E;
@@ -1579,6 +1594,7 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
       // o-proj + residual
       TcGemmParams go = g;
       go.tmap_w = L.tm_o;
+      go.wscale = L.s_o;
       go.tmap_x = F.map_xo;
       go.R = E;
       go.K = qw;
@@ -1589,6 +1605,7 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
       PF_LAUNCH(launch_prep(pp, cs, pdl));
       TcGemmParams gg = g;
       gg.tmap_w = L.tm_gu;
+      gg.wscale = L.s_gu;
       gg.tmap_x = F.map_x;
       gg.R = 2 * ffn;
       gg.K = E;
@@ -1599,6 +1616,7 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
       // down + residual
       TcGemmParams gd = g;
       gd.tmap_w = L.tm_d;
+      gd.wscale = L.s_d;
       gd.tmap_x = F.map_xd;
       gd.R = E;
       gd.K = ffn;
@@ -1761,7 +1779,6 @@ extern "C" int model_prefill(lps_model* m, int b, const int32_t* tokens, int n, 
   if (!m) return fail(LPS_EINVAL, FN, "model is NULL");
   if (m->failed) return fail(LPS_ECUDA, FN, "model is in a failed state after an earlier device error");
   const lps_model_desc& d = m->d;
-  if (m->int8) return fail(LPS_EINVAL, FN, "prefill needs bf16 weights");
   if (m->skinny || m->verify)
     return fail(LPS_EINVAL, FN, "prefill needs the row-major weight layout of a batch-1 model (not batch > 1, "
                                 "not verify rows)");

@@ -46,8 +46,10 @@ using namespace tc;
 constexpr int kTM = 128;                 // weight rows per tile (MMA M)
 constexpr int kKB = 64;                  // K elements per k-block: one 128-byte swizzle row
 constexpr int kATile = kTM * kKB * 2;    // bytes of one weight tile
-constexpr int kThreads = 320;            // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int kThreads = 448;            // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue, 10..13 int8 widening
 constexpr int kEpiThreads = 256;
+constexpr int kCvtThreads = 128;         // warps 10..13
+constexpr int kA8Tile = kTM * kKB;       // bytes of one int8 weight tile (rows of 64 bytes, unswizzled)
 
 // ---- epilogue -------------------------------------------------------------------
 
@@ -125,12 +127,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages, NP = p.NP;
   const int btile = NP * 128;  // bytes of one activation plane's k-block
-  const int stage_bytes = kATile + 2 * btile;
+  // a stage: the bf16 weight tile, the two activation planes, and with int8
+  // weights the raw int8 tile the widening warps turn into the bf16 tile
+  const int stage_bytes = kATile + 2 * btile + (p.int8 ? kA8Tile : 0);
+  const int tx_bytes = (p.int8 ? kA8Tile : kATile) + 2 * btile;  // bytes the copies of a stage bring
+  const int w_off = p.int8 ? kATile + 2 * btile : 0;               // where the weight copy lands
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * stage_bytes);
   uint64_t* empty = full + S;
+  uint64_t* conv = empty + S + 4;  // [S] int8: the bf16 tile of the stage is ready (after acc_full/acc_empty)
   uint64_t* acc_full = empty + S;   // [2]: an accumulator buffer is ready for the epilogue
   uint64_t* acc_empty = acc_full + 2;  // [2]: the epilogue has drained it
-  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(conv + S);
   int* flag = reinterpret_cast<int*>(tmem_base + 1);  // [0]: this CTA finishes the tile
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -150,6 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], kEpiThreads);
     }
+    for (int i = 0; i < S; ++i) mbar_init(&conv[i], 1);
     fence_mbar_init();
   }
   __syncthreads();  // barriers initialised: the producer may start at once
@@ -180,8 +188,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       for (; n < pre; ++n) {
         const long long i = beg + n;
         uint8_t* st = smem + static_cast<size_t>(n) * stage_bytes;
-        mbar_arrive_expect_tx(&full[n], stage_bytes);
-        tma_2d_hint(st, &p.tmap_w, static_cast<int>(i % nkb) * kKB, static_cast<int>(i / nkb) * kTM, &full[n], pol);
+        mbar_arrive_expect_tx(&full[n], tx_bytes);
+        tma_2d_hint(st + w_off, &p.tmap_w, static_cast<int>(i % nkb) * kKB, static_cast<int>(i / nkb) * kTM, &full[n],
+                    pol);
       }
       pdl_wait();
       for (long long m = 0; m < pre; ++m) {
@@ -202,8 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         const long long i = beg + n;
         uint8_t* st = smem + static_cast<size_t>(s) * stage_bytes;
         const int x = static_cast<int>(i % nkb) * kKB;
-        mbar_arrive_expect_tx(&full[s], stage_bytes);
-        tma_2d_hint(st, &p.tmap_w, x, static_cast<int>(i / nkb) * kTM, &full[s], pol);
+        mbar_arrive_expect_tx(&full[s], tx_bytes);
+        tma_2d_hint(st + w_off, &p.tmap_w, x, static_cast<int>(i / nkb) * kTM, &full[s], pol);
         tma_2d(st + kATile, &p.tmap_x, x, 0, &full[s]);
         tma_2d(st + kATile + btile, &p.tmap_x, x, NP, &full[s]);
       }
@@ -232,7 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         const uint32_t d = tbase + static_cast<uint32_t>(b * NP);
         for (int kb = r.k0; kb < r.k1; ++kb, ++n) {
           const int s = static_cast<int>(n % S);
-          if (!mbar_wait(&full[s], static_cast<uint32_t>((n / S) & 1), limit)) {
+          if (!mbar_wait(&full[s], static_cast<uint32_t>((n / S) & 1), limit) ||
+              (p.int8 && !mbar_wait(&conv[s], static_cast<uint32_t>((n / S) & 1), limit))) {
             report_error(p.status, kErrWaitFull | (kKidTcGemm << 8));
             ok = false;
             break;
@@ -252,6 +262,60 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         if (!ok) break;
         umma_commit(&acc_full[b]);
       }
+    }
+  } else if (warp >= 10) {
+    // ---------------- int8 weights: widening warps 10..13 ----------------
+    // Stage s's raw tile (128 rows of 64 int8) becomes the bf16 tile in the
+    // 128-byte-swizzled K-major layout (int8 values are exact in bf16; the row
+    // scale multiplies the accumulator in the epilogue). The stage's bf16 tile
+    // is free again only when the MMAs of its previous use completed, which
+    // the producer already waited for before it refilled the stage.
+    if (p.int8) {
+      const int ct = tid - 320;  // 0..127
+      const long long n_it = end - beg;
+      bool bad = false;
+      for (long long n = 0; n < n_it; ++n) {
+        const int s = static_cast<int>(n % S);
+        const bool got = mbar_wait(&full[s], static_cast<uint32_t>((n / S) & 1), limit);
+        // the four warps leave together on a timeout
+        uint32_t any;
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\t"
+            "setp.ne.u32 p, %1, 0;\n\t"
+            "bar.red.or.pred q, 4, %2, p;\n\t"
+            "selp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(any)
+            : "r"(static_cast<uint32_t>(!got)), "n"(kCvtThreads)
+            : "memory");
+        if (any) {
+          bad = true;
+          break;
+        }
+        uint8_t* st = smem + static_cast<size_t>(s) * stage_bytes;
+        const uint8_t* raw = st + w_off;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int id = ct + kCvtThreads * i, r = id >> 3, ch = id & 7;
+          const uint2 q = *reinterpret_cast<const uint2*>(raw + r * kKB + ch * 8);
+          const uint32_t w4[2] = {q.x, q.y};
+          uint32_t out[4];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int8_t b0 = static_cast<int8_t>(w4[h] & 0xff), b1 = static_cast<int8_t>((w4[h] >> 8) & 0xff);
+            const int8_t b2 = static_cast<int8_t>((w4[h] >> 16) & 0xff), b3 = static_cast<int8_t>(w4[h] >> 24);
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(static_cast<float>(b0), static_cast<float>(b1));
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(static_cast<float>(b2), static_cast<float>(b3));
+            out[2 * h] = *reinterpret_cast<const uint32_t*>(&lo);
+            out[2 * h + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+          }
+          *reinterpret_cast<uint4*>(st + r * 128 + ((ch ^ (r & 7)) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+        }
+        // the tensor core reads the tile through the async proxy
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        named_bar_sync(4, kCvtThreads);
+        if (ct == 0) mbar_arrive(&conv[s]);
+      }
+      (void)bad;
     }
   } else {
     // ---------------- epilogue: warps 2..9 ----------------
@@ -292,6 +356,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         float v[16], w[16];
         tmem_ld16(tacc + static_cast<uint32_t>(c0), v);
         if (whole) {
+          const float sr = (p.wscale && row < p.R) ? p.wscale[row] : 1.f;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] *= sr;
 #pragma unroll
           for (int e = 0; e < 16; ++e) w[e] = __shfl_xor_sync(0xffffffffu, v[e], 1);
           epilogue16(p, row, c0, v, w);
@@ -334,6 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 #pragma unroll
           for (int e = 0; e < 16; ++e) y[e] += t[e];
         }
+        const float sr = (p.wscale && row < p.R) ? p.wscale[row] : 1.f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) y[e] *= sr;
 #pragma unroll
         for (int e = 0; e < 16; ++e) w[e] = __shfl_xor_sync(0xffffffffu, y[e], 1);
         epilogue16(p, row, c0, y, w);
@@ -357,10 +427,10 @@ int tc_gemm_tiles(int R) { return (R + kTM - 1) / kTM; }
 
 // Ring depth from the shared memory: one stage is a 16 KB weight tile and the
 // two activation planes of the same k-block (NP rows of 128 bytes each).
-TcGemmPlan tc_gemm_plan(int NP, int num_sms, int max_smem) {
+TcGemmPlan tc_gemm_plan(int NP, bool int8, int num_sms, int max_smem) {
   TcGemmPlan g{};
   if (NP < 32 || NP > kTcMaxTokens || NP % 32) return g;
-  const int stage = kATile + 2 * NP * 128;
+  const int stage = kATile + 2 * NP * 128 + (int8 ? kA8Tile : 0);
   const int fixed = 1024 + 64 * 8 + 16;  // alignment slack, barriers, TMEM address and flags
   int stages = (max_smem - fixed) / stage;
   stages = stages > 8 ? 8 : stages;

@@ -15,6 +15,9 @@ pytestmark = pytest.mark.gpu
 TINY = synth.CONFIGS["tiny"]
 
 
+TINY_Q8 = TINY.replace(name="tiny_q8", index=97, weight_dtype="int8")
+
+
 @pytest.fixture(scope="module")
 def tiny():
     w = synth.make_weights(TINY)
@@ -165,6 +168,67 @@ def test_8b_prefill_over_oracle_cache():
     assert np.array_equal(dec4, dec1)
 
 
+@pytest.fixture(scope="module")
+def tiny_q8():
+    w = synth.make_weights(TINY_Q8)
+    T = 80
+    toks = synth.make_tokens(TINY_Q8, T)
+    orc = oracle.Oracle(TINY_Q8, w, max_ctx=T)
+    ref = np.stack([orc.step(toks[t], t) for t in range(T)])
+    orc.close()
+    return w, toks, ref
+
+
+def test_tiny_q8_prefill_every_position_and_plans(tiny_q8):
+    """int8 row-scale weights (widened to bf16 in shared memory, the row scale
+    on the accumulator): every prompt position against the oracle at the int8
+    tolerance, decode after the prefill, and bit-identity across stage plans."""
+    w, toks, ref = tiny_q8
+    m = bind(TINY_Q8, w, max_ctx=80)
+    pos, i = 0, 0
+    lens = (3, 16, 1, 21, 7, 16)
+    while pos < 64:
+        n = min(lens[i % len(lens)], 64 - pos)
+        assert_close(m.prefill(toks[pos:pos + n], pos0=pos, chunk=16), ref[pos + n - 1], TINY_Q8,
+                     f"int8 prefill ending at position {pos + n - 1}")
+        pos += n
+        i += 1
+    for t in range(64, 80):
+        assert_close(m.decode_step(toks[t], t), ref[t], TINY_Q8, f"int8 decode step {t} after prefill")
+    base = _prefill_run(TINY_Q8, w, toks, 64, 8, fence=(0, 4))
+    for fence in ((0, 2, 4), (0, 1, 2, 3, 4)):
+        got = _prefill_run(TINY_Q8, w, toks, 64, 8, fence=fence)
+        assert np.array_equal(got[0], base[0]), fence
+        for (kg, vg), (kb, vb) in zip(got[1], base[1]):
+            assert np.array_equal(kg, kb) and np.array_equal(vg, vb), fence
+        assert np.array_equal(got[2], base[2]), fence
+
+
+def test_8b_q8_prefill_over_oracle_cache():
+    """The 8B shape with int8 weights (2 stages, cut 16): one-token prefills over
+    the oracle's own cache rows against the oracle's steps, and a 256-token
+    prefill on 2 stages bit-identical to 1 stage."""
+    cfg = synth.CONFIGS["8b_q8"]
+    P = 128
+    w = synth.make_weights(cfg)
+    toks = synth.make_tokens(cfg, P)
+    orc = oracle.Oracle(cfg, w, max_ctx=P)
+    ref = np.stack([orc.step(toks[t], t) for t in range(P)])
+    kv = [orc.kv_export(l, 0) for l in range(cfg.n_layers)]
+    orc.close()
+    m = bind(cfg, w, max_ctx=P)
+    for t in (0, 5, 64, P - 1):
+        for l in range(cfg.n_layers):
+            m.kv_import(l, 0, kv[l][0], kv[l][1], t)
+        assert_close(m.prefill(toks[t:t + 1], pos0=t), ref[t], cfg, f"8B int8 one-token prefill at {t}")
+    m.close()
+    lg2 = _prefill_run(cfg, w, toks, P, 0, chunk=0)
+    lg1 = _prefill_run(cfg, w, toks, P, 0, fence=(0, cfg.n_layers), chunk=0)
+    assert np.array_equal(lg2[0], lg1[0])
+    for (kg, vg), (kb, vb) in zip(lg2[1], lg1[1]):
+        assert np.array_equal(kg, kb) and np.array_equal(vg, vb)
+
+
 def test_prefill_argument_checks(tiny):
     w, toks, _, _ = tiny
     m = bind(TINY, w, max_ctx=80)
@@ -181,11 +245,6 @@ def test_prefill_argument_checks(tiny):
             m.prefill(**kw)
         assert ei.value.code == lps.LPS_EINVAL, kw
     m.prefill(toks[:4])  # the model is still usable
-    q8 = synth.CONFIGS["tiny"].replace(name="tiny_q8", weight_dtype="int8")
-    mq = bind(q8, synth.make_weights(q8), max_ctx=16)
-    with pytest.raises(lps.LpsError) as ei:
-        mq.prefill(toks[:4])
-    assert ei.value.code == lps.LPS_EINVAL and "bf16" in str(ei.value)
     vm = bind(TINY.replace(name="tiny_v2", batch=2), w, max_ctx=16, flags=lps.LPS_FLAG_VERIFY)
     with pytest.raises(lps.LpsError) as ei:
         vm.prefill(toks[:4])
