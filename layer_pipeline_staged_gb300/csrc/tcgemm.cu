@@ -137,7 +137,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   uint64_t* conv = empty + S + 4;  // [S] int8: the bf16 tile of the stage is ready (after acc_full/acc_empty)
   uint64_t* acc_full = empty + S;   // [2]: an accumulator buffer is ready for the epilogue
   uint64_t* acc_empty = acc_full + 2;  // [2]: the epilogue has drained it
-  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(conv + S);
+  uint64_t* mma_done = conv + S;  // the MMA lane's own MMAs have all completed (before TMEM is freed)
+  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(mma_done + 1);
   int* flag = reinterpret_cast<int*>(tmem_base + 1);  // [0]: this CTA finishes the tile
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -158,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       mbar_init(&acc_empty[i], kEpiThreads);
     }
     for (int i = 0; i < S; ++i) mbar_init(&conv[i], 1);
+    mbar_init(mma_done, 1);
     fence_mbar_init();
   }
   __syncthreads();  // barriers initialised: the producer may start at once
@@ -262,6 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         if (!ok) break;
         umma_commit(&acc_full[b]);
       }
+      // every MMA issued has completed before the accumulators are freed, also
+      // when a wait above gave up and the epilogue never read them
+      umma_commit(mma_done);
+      if (!mbar_wait(mma_done, 0, kDrainLimitCycles)) report_error(p.status, kErrDrain | (kKidTcGemm << 8) | (3 << 13));
     }
   } else if (warp >= 10) {
     // ---------------- int8 weights: widening warps 10..13 ----------------

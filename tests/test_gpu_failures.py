@@ -154,3 +154,32 @@ def test_device_wait_limit_reports_the_kernel(batch, flags, kernel):
     assert_close(m2.decode_step(toks[1], 1), orc.step(toks[1], 1), cfg, "after a failed model")
     with pytest.raises(lps.LpsError):
         m2.set_wait_limit(-1)
+
+
+def test_prefill_device_wait_limit_reports_the_kernel():
+    """The prefill kernels' bounded waits (tcgen05 GEMM ring and accumulators,
+    chunk-attention ring) run out under a 1-cycle limit: the call returns
+    LPS_ECUDA naming a prefill kernel, every issued copy and MMA has landed
+    before the CTAs ended, and the GPU stays usable for a new model."""
+    cfg = WAITCFG
+    w = synth.make_weights(cfg)
+    toks = synth.make_tokens(cfg, 48)
+    m = bind(cfg, w, max_ctx=64)
+    first = m.prefill(toks, chunk=16)
+    m.set_wait_limit(1)
+    with pytest.raises(lps.LpsError) as ei:
+        m.prefill(toks, chunk=16)
+    assert ei.value.code == lps.LPS_ECUDA
+    msg = str(ei.value)
+    assert "device-side error in prefill" in msg and "timed out" in msg, msg
+    with pytest.raises(lps.LpsError) as ei:
+        m.prefill(toks, chunk=16)
+    assert ei.value.code == lps.LPS_ECUDA and "failed state" in str(ei.value)
+    m.close()
+    m2 = bind(cfg, w, max_ctx=64)
+    assert np.array_equal(m2.prefill(toks, chunk=16), first)
+    orc = oracle.Oracle(cfg, w, max_ctx=64)
+    for t in range(len(toks)):
+        ref = orc.step(toks[t], t)
+    assert_close(first, ref, cfg, "prefill before the failure")
+    m2.close()
