@@ -12,10 +12,12 @@
 //     the 128-byte swizzle, which is the canonical K-major layout the MMA reads;
 //   - B = the activations as two bf16 planes, X = hi + lo with hi = bf16(x) and
 //     lo = bf16(x - hi): rows [0, NP) hold hi, rows [NP, 2 NP) lo, so every
-//     activation keeps about 16 significant bits. Each k-step issues two MMAs
-//     (A.hi, A.lo) into the same fp32 accumulator;
-//   - D = 128 weight rows x NP token columns of fp32 in TMEM, two buffers, so
-//     the MMAs of the next tile run while the epilogue drains the last one.
+//     activation keeps about 16 significant bits. The two planes are one
+//     operand of 2 NP rows: each k-step is one MMA with N = 2 NP;
+//   - D = 128 weight rows x 2 NP columns of fp32 in TMEM (column j the hi part
+//     of token j, column NP + j its lo part, added in the epilogue), two
+//     buffers, so the MMAs of the next tile run while the epilogue drains the
+//     last one.
 //
 // Work split (every SM streams the same number of weight bytes): the tiles'
 // k-blocks (tile-major) are cut into gridDim.x equal contiguous ranges, one
@@ -228,7 +230,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(kTM, NP);
+      // one MMA per 16-element k-step with N = 2 NP: the hi and lo planes lie
+      // one after the other in the stage, 8-row groups 1024 bytes apart, so
+      // one descriptor spans both; accumulator column j holds the hi part of
+      // token j, column NP + j the lo part
+      const uint32_t idesc = idesc_bf16(kTM, 2 * NP);
       long long n = 0;
       bool ok = true;
       Run r;
@@ -240,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           break;
         }
         tc_fence_after();
-        const uint32_t d = tbase + static_cast<uint32_t>(b * NP);
+        const uint32_t d = tbase + static_cast<uint32_t>(b * 2 * NP);
         for (int kb = r.k0; kb < r.k1; ++kb, ++n) {
           const int s = static_cast<int>(n % S);
           if (!mbar_wait(&full[s], static_cast<uint32_t>((n / S) & 1), limit) ||
@@ -251,13 +257,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           }
           tc_fence_after();
           const uint32_t st = smem_u32(smem + static_cast<size_t>(s) * stage_bytes);
-          const uint64_t da = sw128_desc(st), dh = sw128_desc(st + kATile), dl = sw128_desc(st + kATile + btile);
+          const uint64_t da = sw128_desc(st), dh = sw128_desc(st + kATile);
 #pragma unroll
           for (int kk = 0; kk < kKB / 16; ++kk) {
             // +32 bytes along the swizzled row per 16-element k-step (>> 4 in the descriptor)
             const uint64_t adv = static_cast<uint64_t>(2 * kk);
             umma_bf16(d, da + adv, dh + adv, idesc, (kb > r.k0 || kk > 0) ? 1u : 0u);
-            umma_bf16(d, da + adv, dl + adv, idesc, 1u);
           }
           umma_commit(&empty[s]);  // the stage is free once these MMAs have read it
         }
@@ -353,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       if (!got && lane == 0) report_error(p.status, kErrWaitFull | (kKidTcGemm << 8) | (2 << 13));
       if (epi_or(!got)) break;  // the epilogue warps leave together
       tc_fence_after();
-      const uint32_t tacc = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(b * NP);
+      const uint32_t tacc = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(b * 2 * NP);
       const bool whole = r.k0 == 0 && r.k1 == nkb;
       const int row = r.tile * kTM + m;
       // partial slot of this CTA: 0 for its first run, 1 for its last
@@ -361,6 +366,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       for (int c0 = cbeg; c0 < cend; c0 += 16) {
         float v[16], w[16];
         tmem_ld16(tacc + static_cast<uint32_t>(c0), v);
+        tmem_ld16(tacc + static_cast<uint32_t>(NP + c0), w);  // the lo parts
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] += w[e];
         if (whole) {
           const float sr = (p.wscale && row < p.R) ? p.wscale[row] : 1.f;
 #pragma unroll
@@ -442,7 +450,7 @@ TcGemmPlan tc_gemm_plan(int NP, bool int8, int num_sms, int max_smem) {
   stages = stages > 8 ? 8 : stages;
   if (stages < 2) return g;
   int cols = 32;
-  while (cols < 2 * NP) cols *= 2;
+  while (cols < 4 * NP) cols *= 2;  // two accumulators of 2 NP columns
   g.grid = num_sms;
   g.stages = stages;
   g.smem = stages * stage + fixed;
