@@ -254,3 +254,39 @@ def test_prefill_argument_checks(tiny):
     with pytest.raises(lps.LpsError) as ei:
         mb.prefill(toks[:4])
     assert ei.value.code == lps.LPS_EINVAL and "row-major" in str(ei.value)
+
+
+def test_prefill_interleaved_with_deferred_steps(tiny):
+    """Prefill calls enqueued while deferred decode steps are still in flight
+    (stream order keeps them apart): a prompt prefilled, deferred steps, a second
+    prompt segment appended by prefill, more deferred steps -- the same bits at
+    every position as the same schedule run eagerly on another model."""
+    w, toks, _, _ = tiny
+    seq = [("p", 0, 24), ("d", 24, 6), ("p", 30, 20), ("d", 50, 10)]
+
+    def run(deferred):
+        m = bind(TINY, w, max_ctx=80, pending_depth=4)
+        out, pend = {}, []
+        for kind, p0, n in seq:
+            if kind == "p":
+                out[p0 + n - 1] = m.prefill(toks[p0:p0 + n], pos0=p0, chunk=16)
+                continue
+            for t in range(p0, p0 + n):
+                if not deferred:
+                    out[t] = m.decode_step(toks[t], t)
+                    continue
+                pend.append((t, m.decode_step_deferred(toks[t], t)))
+                if len(pend) == 4:
+                    tp, p = pend.pop(0)
+                    out[tp] = p.wait()
+                    p.free()
+        for tp, p in pend:
+            out[tp] = p.wait()
+            p.free()
+        m.close()
+        return out
+
+    eager, deferred = run(False), run(True)
+    assert sorted(eager) == sorted(deferred)
+    for t in eager:
+        assert np.array_equal(eager[t], deferred[t]), t
