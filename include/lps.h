@@ -342,20 +342,26 @@ int model_attn_out(const lps_model* m, int layer, int b, float* host);
 #define LPS_KERNEL_EMBED 6
 #define LPS_KERNEL_STAGE 7  /* the persistent stage kernel (batch 1): one launch per stage and step */
 #define LPS_KERNEL_MERGE 8  /* trace only: the persistent kernel's merge of the attention chunks */
+#define LPS_KERNEL_PF_SPLIT 9   /* trace only: prefill, activation split (with the RMSNorm) */
+#define LPS_KERNEL_PF_GEMM 10   /* trace only: prefill, a tcgen05 projection GEMM */
+#define LPS_KERNEL_PF_ATTN 11   /* trace only: prefill, the chunk attention */
+#define LPS_KERNEL_PF_MERGE 12  /* trace only: prefill, the merge of the chunk attention's key chunks */
 int model_time_kernel(lps_model* m, int kind, int enable);
 int model_kernel_time(lps_model* m, int kind, double* total_ms, uint64_t* launches);
 
 /* ---- launch trace --------------------------------------------------------- */
 
-/* One launch of the decode step: its kernel family, where it ran, and the
- * device clock (%globaltimer, ns) of its earliest CTA start and latest warp
- * end, so that overlapping launches (stages, programmatic dependent launch)
- * show as they ran. */
+/* One launch of a decode step or a prefill chunk: its kernel family, where it
+ * ran, and the device clock (%globaltimer, ns) of its earliest CTA start and
+ * latest warp end, so that overlapping launches (stages, programmatic
+ * dependent launch, consecutive steps or chunks) show as they ran. */
 typedef struct {
   int32_t kind;      /* LPS_KERNEL_* */
   int32_t stage;
   int32_t layer;     /* -1 for the embedding and the LM head */
-  int32_t step;      /* the model's step counter when the launch was enqueued */
+  int32_t step;      /* the model's step counter when the launch was enqueued; for a
+                        prefill launch (the LPS_KERNEL_PF_* kinds, and the embedding
+                        and LM head of a prefill) the model's prefill chunk counter */
   uint64_t start_ns;
   uint64_t end_ns;   /* 0 if the launch has not finished or left early */
 } lps_trace_record;

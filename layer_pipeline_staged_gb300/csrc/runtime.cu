@@ -558,8 +558,9 @@ bool make_i8_map(CUtensorMap* map, const void* base, unsigned long long cols, un
 
 namespace {
 
-// The trace record of the next launch (two zeroed 64-bit words), or nullptr.
-unsigned long long* trace_slot(lps_model* m, int kind, int stage, int layer) {
+// The trace record of the next launch (two zeroed 64-bit words), or nullptr;
+// `step` is the decode step (or, for prefill launches, the chunk) it belongs to.
+unsigned long long* trace_slot_at(lps_model* m, int kind, int stage, int layer, int64_t step) {
   if (!m->trace_dev) return nullptr;
   if (m->trace_n >= m->trace_cap) {
     ++m->trace_dropped;
@@ -569,9 +570,13 @@ unsigned long long* trace_slot(lps_model* m, int kind, int stage, int layer) {
   r.kind = kind;
   r.stage = stage;
   r.layer = layer;
-  r.step = static_cast<int32_t>(m->step_count);
+  r.step = static_cast<int32_t>(step);
   m->trace_meta.push_back(r);
   return m->trace_dev + 2 * static_cast<size_t>(m->trace_n++);
+}
+
+unsigned long long* trace_slot(lps_model* m, int kind, int stage, int layer) {
+  return trace_slot_at(m, kind, stage, layer, static_cast<int64_t>(m->step_count));
 }
 
 // n consecutive trace records (the phases of one persistent launch), or
@@ -1488,6 +1493,8 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
   const int N = m->N, E = d.n_embd, nq = d.n_q_heads, nkv = d.n_kv_heads, hd = d.head_dim, ffn = d.ffn;
   const int qw = nq * hd, NP = P.NP;
   const int par = static_cast<int>(P.chunks & 1);
+  const int64_t chunk_no = static_cast<int64_t>(P.chunks);
+  auto tr = [&](int kind, int stage, int layer) { return trace_slot_at(m, kind, stage, layer, chunk_no); };
   int nchunks = 1, achunk = 1;
   chunk_attn_split(hd, nkv, ntok, pos0, m->num_sms, &nchunks, &achunk);
   uint64_t launches = 0;
@@ -1519,6 +1526,7 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
       ep.batch = ntok;
       ep.h = F.h;
       ep.status = m->status_dev;
+      ep.trace = tr(LPS_KERNEL_EMBED, s, -1);
       PF_LAUNCH(launch_embed(ep, m->int8, cs, pdl));
     } else {
       CK(cudaMemcpyAsync(F.h, P.bd[s - 1].slot[par], sizeof(float) * ntok * E, cudaMemcpyDeviceToDevice, cs),
@@ -1556,6 +1564,7 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
       const LayerDev& L = S.layers[i];
       // RMSNorm -> QKV -> RoPE -> q and the chunk's cache rows
       pp.gain = L.attn_norm;
+      pp.trace = tr(LPS_KERNEL_PF_SPLIT, s, l);
       PF_LAUNCH(launch_prep(pp, cs, pdl));
       TcGemmParams gq = g;
       gq.tmap_w = L.tm_qkv;
@@ -1567,6 +1576,7 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
       gq.q = F.q;
       gq.kc = L.kc;
       gq.vc = L.vc;
+      gq.trace = tr(LPS_KERNEL_PF_GEMM, s, l);
       PF_LAUNCH(launch_tc_gemm(gq, P.plan, cs, pdl));
       // causal attention of the chunk, merged into the o-proj input planes
       ChunkAttnParams ap{};
@@ -1589,6 +1599,8 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
       ap.scale = 1.0f / std::sqrt(static_cast<float>(hd));
       ap.wait_limit = m->wait_limit;
       ap.status = m->status_dev;
+      ap.trace = tr(LPS_KERNEL_PF_ATTN, s, l);
+      ap.trace_merge = tr(LPS_KERNEL_PF_MERGE, s, l);
       PF_LAUNCH(launch_chunk_attn(ap, cs, pdl));
       ++launches;  // the merge
       // o-proj + residual
@@ -1599,9 +1611,11 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
       go.R = E;
       go.K = qw;
       go.epi = kEpiResidual;
+      go.trace = tr(LPS_KERNEL_PF_GEMM, s, l);
       PF_LAUNCH(launch_tc_gemm(go, P.plan, cs, pdl));
       // RMSNorm -> gate/up -> SwiGLU (into the down projection's input planes)
       pp.gain = L.ffn_norm;
+      pp.trace = tr(LPS_KERNEL_PF_SPLIT, s, l);
       PF_LAUNCH(launch_prep(pp, cs, pdl));
       TcGemmParams gg = g;
       gg.tmap_w = L.tm_gu;
@@ -1612,6 +1626,7 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
       gg.epi = kEpiSwiglu;
       gg.xo = F.xd;
       gg.ldx = ffn;
+      gg.trace = tr(LPS_KERNEL_PF_GEMM, s, l);
       PF_LAUNCH(launch_tc_gemm(gg, P.plan, cs, pdl));
       // down + residual
       TcGemmParams gd = g;
@@ -1621,6 +1636,7 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
       gd.R = E;
       gd.K = ffn;
       gd.epi = kEpiResidual;
+      gd.trace = tr(LPS_KERNEL_PF_GEMM, s, l);
       PF_LAUNCH(launch_tc_gemm(gd, P.plan, cs, pdl));
     }
     if (s + 1 < N) {
@@ -1650,6 +1666,7 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
     p.out = m->eager_logits_dev;
     p.status = m->status_dev;
     p.wait_limit = m->wait_limit;
+    p.trace = tr(LPS_KERNEL_HEAD, N - 1, -1);
     PF_LAUNCH(launch_gemv(p, kEpiStore, true, m->int8, S.plan_head, cs, pdl));
   }
 #undef PF_LAUNCH

@@ -75,3 +75,44 @@ def test_trace_capacity_counts_dropped_launches(flags):
     kept = 1 + 6 * TINY.fence[1] if flags else 5
     assert len(recs) == kept and dropped == len(per_step) - kept
     m.trace_disable()
+
+
+def test_trace_records_prefill_chunks_through_the_stages():
+    """A 3-chunk prefill on 2 stages: every launch recorded with its chunk
+    number; per chunk, stage 0 runs the embedding and its layers, stage 1 its
+    layers (split, QKV GEMM, chunk attention, merge, o-proj GEMM, split, gate/up
+    GEMM, down GEMM per layer), the last chunk ends with the LM head; stage 1
+    starts chunk c only after stage 0 has finished it (the boundary slot's
+    event). Tracing changes no result."""
+    w = synth.make_weights(TINY)
+    toks = synth.make_tokens(TINY, 48)
+    plain = bind(TINY, w, max_ctx=48).prefill(toks, chunk=16)
+    m = bind(TINY, w, max_ctx=48)
+    m.prefill(toks[:16], chunk=16)  # the first call allocates the prefill buffers
+    m.trace_enable(4096)
+    got = m.prefill(toks, chunk=16)
+    recs, dropped = m.trace_read()
+    assert dropped == 0 and np.array_equal(got, plain)
+    layer = ["pf_split", "pf_gemm", "pf_attn", "pf_merge", "pf_gemm", "pf_split", "pf_gemm", "pf_gemm"]
+    fence = TINY.fence
+    chunks = sorted({r["step"] for r in recs})
+    assert len(chunks) == 3
+    for i, c in enumerate(chunks):
+        for s in range(len(fence) - 1):
+            rs = [r for r in recs if r["step"] == c and r["stage"] == s and r["kind"] != "head"]
+            want = (["embed"] if s == 0 else []) + layer * (fence[s + 1] - fence[s])
+            assert [r["kind"] for r in rs] == want, (c, s)
+            assert all(0 < r["start_ns"] <= r["end_ns"] for r in rs)
+        s0 = [r for r in recs if r["step"] == c and r["stage"] == 0]
+        s1 = [r for r in recs if r["step"] == c and r["stage"] == 1 and r["kind"] != "head"]
+        assert min(r["start_ns"] for r in s1) >= max(r["end_ns"] for r in s0), c
+    heads = [r for r in recs if r["kind"] == "head"]
+    assert len(heads) == 1 and heads[0]["step"] == chunks[-1]
+    # report how much of stage 1's chunk c ran while stage 0 ran chunk c + 1
+    for a, b in zip(chunks, chunks[1:]):
+        s1 = [r for r in recs if r["step"] == a and r["stage"] == 1 and r["kind"] != "head"]
+        s0 = [r for r in recs if r["step"] == b and r["stage"] == 0]
+        lo = max(min(r["start_ns"] for r in s1), min(r["start_ns"] for r in s0))
+        hi = min(max(r["end_ns"] for r in s1), max(r["end_ns"] for r in s0))
+        print(f"chunks {a}/{b}: stage 1 and stage 0 overlap for {max(0, hi - lo) / 1e3:.1f} us")
+    m.trace_disable()
