@@ -8,7 +8,7 @@ import pytest
 import layer_pipeline_staged_gb300 as lps
 import oracle
 import synth
-from workloads import assert_close, bind
+from workloads import assert_close, bind, random_kv
 
 pytestmark = pytest.mark.gpu
 
@@ -290,3 +290,37 @@ def test_prefill_interleaved_with_deferred_steps(tiny):
     assert sorted(eager) == sorted(deferred)
     for t in eager:
         assert np.array_equal(eager[t], deferred[t]), t
+
+
+MID = synth.ModelConfig("mid_prefill", 93, 3, 512, 32, 8, 128, 512, 1000, "bf16", 1, 0, 0, (1, 2))
+
+
+@pytest.mark.parametrize("chunk", [16, 0])
+def test_prefill_after_long_imported_context(chunk):
+    """Cache rows [0, 5000) imported into both sides, then 40 prompt tokens
+    prefilled in calls of 17, 1 and 22 tokens: the chunk attention runs over
+    many key chunks per 16-token block, with the causal mask inside the chunk;
+    each call's last logits against the oracle's step at that position, and
+    the cache rows the prefill wrote against the oracle's."""
+    cfg, P = MID, 5000
+    w = synth.make_weights(cfg)
+    max_ctx = P + 40
+    orc = oracle.Oracle(cfg, w, max_ctx=max_ctx)
+    m = bind(cfg, w, max_ctx=max_ctx)
+    for (l, b), (k, v) in random_kv(cfg, 19, cfg.n_layers, max_ctx, P).items():
+        m.kv_import(l, b, k, v, P)
+        orc.kv_import(l, b, k, v, P)
+    toks = synth.make_tokens(cfg, 40, seed=61)[:, 0]
+    ref = [orc.step(toks[j:j + 1], P + j)[0] for j in range(40)]
+    pos = 0
+    for n in (17, 1, 22):
+        got = m.prefill(toks[pos:pos + n], pos0=P + pos, chunk=chunk)
+        assert_close(got, ref[pos + n - 1], cfg, f"prefill ending at {P + pos + n - 1}")
+        pos += n
+    for l in range(cfg.n_layers):
+        for a, b in zip(m.kv_export(l, 0), orc.kv_export(l, 0)):
+            assert np.array_equal(a[:, :P], b[:, :P])
+            rg = synth.bf16_to_f32(a[:, P:P + 40]).astype(np.float64)
+            ro = synth.bf16_to_f32(b[:, P:P + 40]).astype(np.float64)
+            scale = np.max(np.abs(ro), axis=2, keepdims=True)
+            assert np.all(np.abs(rg - ro) <= np.abs(ro) * 2 ** -6 + 1e-3 * scale), f"layer {l}"
