@@ -222,7 +222,7 @@ struct ChunkAttnParams {
   float* out;                  // when set: the merged o as fp32 [ntok][nq*hd] instead of the planes
   __nv_bfloat16* xo;
   int nq, nkv, hd, max_ctx, max_chunks;
-  int chunk, nchunks;          // keys per CTA, CTAs per (block, kv head): chunk_attn_split
+  int chunk, nchunks, qblock;  // keys per CTA, CTAs per (block, kv head), tokens per block: chunk_attn_split
   int seq, pos0, ntok, NP;
   float scale;
   long long wait_limit;
@@ -232,7 +232,8 @@ struct ChunkAttnParams {
 };
 int chunk_attn_sub_tile(int hd);
 int chunk_attn_max_chunks(int nkv, int num_sms);
-void chunk_attn_split(int hd, int nkv, int ntok, int pos0, int num_sms, int* nchunks, int* chunk);
+void chunk_attn_split(int hd, int nq, int nkv, int ntok, int pos0, int num_sms, int* nchunks, int* chunk,
+                      int* qblock);
 cudaError_t launch_chunk_attn(const ChunkAttnParams& p, cudaStream_t s, bool pdl);
 
 // ---- persistent stage kernel (batch 1) -----------------------------------------

@@ -9,10 +9,14 @@
 // chunk's own rows (the QKV GEMM wrote them just before). The work is split
 // like the decode attention, by key chunks, so that every SM has work at any
 // context length:
-//   - CTA (key chunk kc, query block qb of 16 tokens, kv head g) runs one warp
-//     per q head of the group; each warp holds its head's 16 query rows as
-//     mma.sync A fragments, split into bf16 hi and lo parts (two MMAs per
-//     k-step), so q keeps about 16 significant bits;
+//   - CTA (key chunk kc, query block qb of up to 128 / G tokens, kv head g)
+//     runs one warp per (q head of the group, 16 tokens of the block), up to
+//     eight: warp w takes head w mod G and the w / G-th 16 tokens, so every K/V
+//     byte the CTA brings in serves all of them (a block is one 16-token group
+//     when the chunk has at most 16 tokens, as verify rows do, which keeps two
+//     CTAs per SM there); each warp holds its 16 query rows as mma.sync A fragments, split
+//     into bf16 hi and lo parts (two MMAs per k-step), so q keeps about 16
+//     significant bits;
 //   - K and V sub-tiles arrive by 2D TMA with the 128-byte swizzle into a
 //     ring shared by the group's warps; keys past a row's own position are
 //     masked; each warp keeps an online softmax per row and accumulates P.V
@@ -184,9 +188,10 @@ __global__ void __launch_bounds__(256) chunk_attn_kernel(const __grid_constant__
   trace_start(p.trace);
   const int kc = blockIdx.x, qb = blockIdx.y, g = blockIdx.z;
   const int G = p.nq / p.nkv, qw = p.nq * HD;
-  const int h = g * G + warp;
-  const int j0 = qb * 16, jn = min(16, p.ntok - j0);  // live query rows of this block
-  const int kend = p.pos0 + j0 + jn;                  // the block attends keys [0, kend)
+  const int h = g * G + warp % G;
+  const int jb = qb * p.qblock;                                      // the CTA's first token
+  const int j0 = jb + (warp / G) * 16, jn = min(16, p.ntok - j0);  // this warp's rows (jn <= 0: none)
+  const int kend = p.pos0 + min(jb + p.qblock, p.ntok);             // the block attends keys [0, kend)
   const int k_begin = kc * p.chunk;
   if (k_begin >= kend) return;  // uniform per CTA: the merge reads no partial of this chunk
   const int k_stop = min(k_begin + p.chunk, kend);
@@ -260,10 +265,15 @@ __global__ void __launch_bounds__(256) chunk_attn_kernel(const __grid_constant__
     }
     const uint32_t kbase = smem_u32(kt + slot * S::TILE), vbase = smem_u32(vt + slot * S::TILE);
     const int tile_key = k_begin + jt * S::TS;
+    // A warp computes only the key groups its rows can see: none when its 16
+    // tokens lie past the chunk, none past its last row's position (the causal
+    // bound; such a group would leave every sum unchanged). It still meets the
+    // other warps at the ring's barrier below.
+    const int kmax = jn > 0 ? p.pos0 + j0 + jn - 1 : -1;  // the warp's last visible key
 #pragma unroll 1
     for (int kg = 0; kg < S::TS / 32; ++kg) {
       const int kb = tile_key + kg * 32;  // first key of this group of 32
-      if (kb >= k_stop) break;
+      if (kb >= k_stop || kb > kmax) break;
       float sc[4][4];
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
@@ -394,8 +404,8 @@ __global__ void __launch_bounds__(256) chunk_merge_kernel(const __grid_constant_
   const int pair = blockIdx.x * 8 + warp;
   if (pair < p.ntok * p.nq) {
     const int j = pair / p.nq, h = pair - j * p.nq, qw = p.nq * HD;
-    const int j0 = (j / 16) * 16, jn = min(16, p.ntok - j0);
-    const int kend = p.pos0 + j0 + jn;
+    const int jb = (j / p.qblock) * p.qblock;
+    const int kend = p.pos0 + min(jb + p.qblock, p.ntok);  // the keys the token's block attended
     const int nch = (kend + p.chunk - 1) / p.chunk;
     const float* base = p.part + (static_cast<size_t>(j) * p.nq + h) * p.max_chunks * (HD + 4);
     float mloc = -INFINITY;
@@ -460,9 +470,8 @@ cudaError_t launch_chunk_attn_t(const ChunkAttnParams& p, cudaStream_t s, bool p
   static std::atomic<int> smem_set[kMaxDevices];
   cudaError_t e = set_smem_attr(chunk_attn_kernel<HD>, smem, smem_set);
   if (e != cudaSuccess) return e;
-  const int G = p.nq / p.nkv;
-  const dim3 grid(p.nchunks, (p.ntok + 15) / 16, p.nkv);
-  e = launch_ex(chunk_attn_kernel<HD>, p, grid, dim3(32 * G), smem, s, pdl);
+  const dim3 grid(p.nchunks, (p.ntok + p.qblock - 1) / p.qblock, p.nkv);
+  e = launch_ex(chunk_attn_kernel<HD>, p, grid, dim3(32 * (p.nq / p.nkv) * (p.qblock / 16)), smem, s, pdl);
   if (e != cudaSuccess) return e;
   ChunkAttnParams q = p;
   q.trace = p.trace_merge;
@@ -479,12 +488,17 @@ int chunk_attn_sub_tile(int hd) { return 8192 / hd; }
 
 int chunk_attn_max_chunks(int nkv, int num_sms) { return (2 * num_sms + nkv - 1) / nkv + 1; }
 
-// Key chunks for a chunk of ntok tokens ending at position pos0 + ntok - 1:
-// about two CTAs per SM over (kv heads x 16-token blocks x key chunks), of
-// whole sub-tiles, none empty.
-void chunk_attn_split(int hd, int nkv, int ntok, int pos0, int num_sms, int* nchunks, int* chunk) {
+// Query blocks (16 tokens per warp row group, G x blocks/16 <= 8 warps per CTA:
+// 128 / G tokens, or 16 when the chunk has at most 16) and key chunks for a
+// chunk of ntok tokens ending at position pos0 + ntok - 1: about two CTAs per
+// SM over (kv heads x query blocks x key chunks), of whole sub-tiles, none
+// empty.
+void chunk_attn_split(int hd, int nq, int nkv, int ntok, int pos0, int num_sms, int* nchunks, int* chunk,
+                      int* qblock) {
   const int ts = chunk_attn_sub_tile(hd);
-  const int nqb = (ntok + 15) / 16;
+  const int groups16 = (ntok + 15) / 16, per_cta = 8 / (nq / nkv);
+  *qblock = 16 * (groups16 < per_cta ? groups16 : per_cta);
+  const int nqb = (ntok + *qblock - 1) / *qblock;
   const int kend = pos0 + ntok;
   const int nsub = (kend + ts - 1) / ts;
   int target = (2 * num_sms + nkv * nqb - 1) / (nkv * nqb);
@@ -498,8 +512,9 @@ void chunk_attn_split(int hd, int nkv, int ntok, int pos0, int num_sms, int* nch
 }
 
 cudaError_t launch_chunk_attn(const ChunkAttnParams& p, cudaStream_t s, bool pdl) {
-  if (p.nq % p.nkv || p.nq / p.nkv > 8 || p.nq / p.nkv < 1 || p.ntok < 1 || p.ntok > kTcMaxTokens ||
-      p.max_chunks > kMaxMergeChunks || p.nchunks > p.max_chunks)
+  if (p.nq % p.nkv || p.nq / p.nkv > 8 || p.nq / p.nkv < 1 || 8 % (p.nq / p.nkv) || p.ntok < 1 ||
+      p.ntok > kTcMaxTokens || p.max_chunks > kMaxMergeChunks || p.nchunks > p.max_chunks ||
+      p.qblock < 16 || p.qblock % 16 || (p.nq / p.nkv) * (p.qblock / 16) > 8)
     return cudaErrorInvalidValue;
   if (p.hd == 128) return launch_chunk_attn_t<128>(p, s, pdl);
   if (p.hd == 64) return launch_chunk_attn_t<64>(p, s, pdl);

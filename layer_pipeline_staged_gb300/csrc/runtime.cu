@@ -1277,7 +1277,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
           cp.hd = hd;
           cp.max_ctx = d.max_ctx;
           cp.max_chunks = chunk_attn_max_chunks(nkv, m->num_sms);
-          chunk_attn_split(hd, nkv, B, pos[0], m->num_sms, &cp.nchunks, &cp.chunk);
+          chunk_attn_split(hd, nq, nkv, B, pos[0], m->num_sms, &cp.nchunks, &cp.chunk, &cp.qblock);
           cp.seq = 0;
           cp.pos0 = pos[0];
           cp.ntok = B;
@@ -1495,8 +1495,8 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
   const int par = static_cast<int>(P.chunks & 1);
   const int64_t chunk_no = static_cast<int64_t>(P.chunks);
   auto tr = [&](int kind, int stage, int layer) { return trace_slot_at(m, kind, stage, layer, chunk_no); };
-  int nchunks = 1, achunk = 1;
-  chunk_attn_split(hd, nkv, ntok, pos0, m->num_sms, &nchunks, &achunk);
+  int nchunks = 1, achunk = 1, qblock = 16;
+  chunk_attn_split(hd, nq, nkv, ntok, pos0, m->num_sms, &nchunks, &achunk, &qblock);
   uint64_t launches = 0;
   bool pdl = false;
 #define PF_LAUNCH(call)                                 \
@@ -1592,6 +1592,7 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
       ap.max_chunks = P.max_chunks;
       ap.chunk = achunk;
       ap.nchunks = nchunks;
+      ap.qblock = qblock;
       ap.seq = seq;
       ap.pos0 = pos0;
       ap.ntok = ntok;
