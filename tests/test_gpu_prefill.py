@@ -324,3 +324,39 @@ def test_prefill_after_long_imported_context(chunk):
             ro = synth.bf16_to_f32(b[:, P:P + 40]).astype(np.float64)
             scale = np.max(np.abs(ro), axis=2, keepdims=True)
             assert np.all(np.abs(rg - ro) <= np.abs(ro) * 2 ** -6 + 1e-3 * scale), f"layer {l}"
+
+
+G8 = synth.ModelConfig("g8_prefill", 88, 2, 512, 16, 2, 64, 512, 1000, "bf16", 1, 0, 0, (1,))
+G1 = synth.ModelConfig("g1_prefill", 89, 2, 512, 4, 4, 128, 512, 1000, "bf16", 1, 0, 0, (1,))
+
+
+@pytest.mark.parametrize("cfg", [G8, G1], ids=lambda c: c.name)
+def test_prefill_group_sizes(cfg):
+    """The chunk attention at the GQA extremes: eight q heads per kv head (one
+    16-token group per CTA, eight warps) and one (eight 16-token groups per
+    CTA), after 700 imported cache rows; each call's last logits against the
+    oracle, and two stage plans bit-identical."""
+    P = 700
+    w = synth.make_weights(cfg)
+    max_ctx = P + 40
+    orc = oracle.Oracle(cfg, w, max_ctx=max_ctx)
+    kv = random_kv(cfg, 23, cfg.n_layers, max_ctx, P)
+    toks = synth.make_tokens(cfg, 40, seed=62)[:, 0]
+    for (l, b), (k, v) in kv.items():
+        orc.kv_import(l, b, k, v, P)
+    ref = [orc.step(toks[j:j + 1], P + j)[0] for j in range(40)]
+    outs = []
+    for fence in ((0, 1, 2), (0, 2)):
+        m = bind(cfg, w, fence=fence, max_ctx=max_ctx)
+        for (l, b), (k, v) in kv.items():
+            m.kv_import(l, b, k, v, P)
+        got, pos = [], 0
+        for n in (17, 1, 22):
+            lg = m.prefill(toks[pos:pos + n], pos0=P + pos, chunk=0)
+            assert_close(lg, ref[pos + n - 1], cfg, f"{cfg.name} prefill ending at {P + pos + n - 1}")
+            got.append(lg)
+            pos += n
+        outs.append(got)
+        m.close()
+    for a, b in zip(outs[0], outs[1]):
+        assert np.array_equal(a, b)
