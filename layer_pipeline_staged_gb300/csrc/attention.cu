@@ -516,16 +516,25 @@ static int attn_chunk_model(int nsub, long long groups, int num_sms, int slots) 
   return best_cs;
 }
 
-// Balancing the bytes per SM (one CTA slot per SM in the model) gives fewer
-// partials to merge and measured faster, except where it leaves one CTA per
-// SM with a long chunk: its four warps are then latency-bound, and two
-// resident CTAs per SM with half the chunk measured faster (8B shapes: one
-// slot wins at context 8192 batch 1 and at context 4096 batch 4, two slots
+// Otherwise balancing the bytes per SM (one CTA slot per SM in the model)
+// gives fewer partials to merge and measured faster, except where it leaves
+// one CTA per SM with a long chunk: its four warps are then latency-bound, and
+// two resident CTAs per SM with half the chunk measured faster (8B shapes: one
+// slot wins at context 4096 batch 4 and at context 32768 batch 8, two slots
 // at context 32768 batch 1).
 int attn_chunk(int hd, int nkv, int batch, int max_pos, int num_sms) {
   const int ts = attn_sub_tile(hd);
   const int nsub = (max_pos + 1 + ts - 1) / ts;  // sub-tiles of one (sequence, kv head)
   const long long groups = static_cast<long long>(nkv) * batch;
+  if (batch == 1 && nsub <= 256) {
+    // one sequence, up to 256 sub-tiles: about one CTA per two SMs. In the
+    // overlapped step the other stages' projections take the remaining SMs;
+    // measured on the 8B bf16 step at context 8192 (4 stages): 2.901 ms with 152
+    // CTAs of 7 sub-tiles, 2.880-2.885 with 64-88 CTAs of 12-16, 2.997 with 32
+    const long long per = (num_sms + groups) / (2 * groups);
+    const int chunks = static_cast<int>(per < 1 ? 1 : per);
+    return (nsub + chunks - 1) / chunks * ts;
+  }
   const int cs1 = attn_chunk_model(nsub, groups, num_sms, 1);
   const long long ctas1 = groups * ((nsub + cs1 - 1) / cs1);
   if (cs1 <= 24 || ctas1 > num_sms) return cs1 * ts;
