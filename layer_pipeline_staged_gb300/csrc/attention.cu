@@ -522,16 +522,17 @@ static int attn_chunk_model(int nsub, long long groups, int num_sms, int slots) 
 // two resident CTAs per SM with half the chunk measured faster (8B shapes: one
 // slot wins at context 4096 batch 4 and at context 32768 batch 8, two slots
 // at context 32768 batch 1).
-int attn_chunk(int hd, int nkv, int batch, int max_pos, int num_sms, bool shared) {
+int attn_chunk(int hd, int nkv, int batch, int max_pos, int num_sms) {
   const int ts = attn_sub_tile(hd);
   const int nsub = (max_pos + 1 + ts - 1) / ts;  // sub-tiles of one (sequence, kv head)
   const long long groups = static_cast<long long>(nkv) * batch;
-  if (shared && batch == 1 && nsub <= 256) {
-    // one sequence, up to 256 sub-tiles, and other stages' kernels running
-    // beside this one (`shared`): about one CTA per two SMs, the other stages'
-    // projections take the rest; measured on the 8B bf16 step at context 8192
-    // (4 stages): 2.901 ms with 152 CTAs of 7 sub-tiles, 2.880-2.885 with
-    // 64-88 CTAs of 12-16, 2.997 with 32
+  if (batch == 1 && nsub <= 256) {
+    // one sequence, up to 256 sub-tiles: about one CTA per two SMs, so that
+    // other stages' kernels can run beside it; measured on the 8B bf16 step at
+    // context 8192 (4 stages): 2.901 ms with 152 CTAs of 7 sub-tiles,
+    // 2.880-2.885 with 64-88 CTAs of 12-16, 2.997 with 32. The chunking depends
+    // on the shapes, the position and the SM count only (never on the stage
+    // plan), so every plan sums the same partials in the same order
     const long long per = (num_sms + groups) / (2 * groups);
     const int chunks = static_cast<int>(per < 1 ? 1 : per);
     return (nsub + chunks - 1) / chunks * ts;
@@ -544,12 +545,11 @@ int attn_chunk(int hd, int nkv, int batch, int max_pos, int num_sms, bool shared
 
 int attn_max_chunks(int hd, int nkv, int batch, int max_ctx, int num_sms) {
   int worst = 1;
-  for (int n = 1; n <= max_ctx; ++n)
-    for (bool shared : {false, true}) {
-      const int ch = attn_chunk(hd, nkv, batch, n - 1, num_sms, shared);
-      const int k = (n + ch - 1) / ch;
-      worst = k > worst ? k : worst;
-    }
+  for (int n = 1; n <= max_ctx; ++n) {
+    const int ch = attn_chunk(hd, nkv, batch, n - 1, num_sms);
+    const int k = (n + ch - 1) / ch;
+    worst = k > worst ? k : worst;
+  }
   return worst;
 }
 

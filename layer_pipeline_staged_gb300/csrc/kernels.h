@@ -148,9 +148,9 @@ struct AttnParams {
   unsigned long long* trace;  // launch trace record, or nullptr
 };
 int attn_sub_tile(int hd);
-// Positions per attention CTA at max_pos; `shared`: other stages' kernels run
-// beside the attention (overlapping stages), which favours fewer, longer chunks.
-int attn_chunk(int hd, int nkv, int batch, int max_pos, int num_sms, bool shared = false);
+// Positions per attention CTA at max_pos (a function of the shapes, the
+// position and the SM count only, so every stage plan gets the same bits).
+int attn_chunk(int hd, int nkv, int batch, int max_pos, int num_sms);
 int attn_max_chunks(int hd, int nkv, int batch, int max_ctx, int num_sms);
 cudaError_t launch_attention(const AttnParams& p, int batch, int max_pos, cudaStream_t s, bool pdl);
 

@@ -36,7 +36,7 @@
 #include "lps.h"
 
 namespace lps {
-int attn_chunk(int hd, int nkv, int batch, int max_pos, int num_sms, bool shared);
+int attn_chunk(int hd, int nkv, int batch, int max_pos, int num_sms);
 int attn_sub_tile(int hd);
 bool attn_supported(int hd, int group);
 }  // namespace lps
@@ -128,7 +128,7 @@ extern "C" long long attention_decode_noalloc_scratch_bytes(int batch, int n_q_h
     cudaGetLastError();
     return -1;
   }
-  const int chunk = attn_chunk(head_dim, n_kv_heads, batch, max_pos, num_sms, false);
+  const int chunk = attn_chunk(head_dim, n_kv_heads, batch, max_pos, num_sms);
   size_t counter_bytes = 0, part_bytes = 0;
   scratch_need(batch, n_q_heads, n_kv_heads, head_dim, (max_pos + 1 + chunk - 1) / chunk, &counter_bytes, &part_bytes);
   return static_cast<long long>(counter_bytes + part_bytes);
@@ -161,7 +161,7 @@ extern "C" int attention_decode_noalloc(const float* q, const void* k_cache, con
   e = scratch_on(dev, &base, &num_sms);
   if (e != cudaSuccess) return fail(LPS_ECUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
 
-  const int chunk = attn_chunk(head_dim, n_kv_heads, batch, max_pos, num_sms, false);
+  const int chunk = attn_chunk(head_dim, n_kv_heads, batch, max_pos, num_sms);
   const int nchunks = (max_pos + 1 + chunk - 1) / chunk;
   size_t counter_bytes = 0, part_bytes = 0;
   scratch_need(batch, n_q_heads, n_kv_heads, head_dim, nchunks, &counter_bytes, &part_bytes);

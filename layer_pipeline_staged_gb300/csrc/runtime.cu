@@ -1151,9 +1151,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
   const int par = static_cast<int>(m->step_count & 1);
   int max_pos = 0;
   for (int b = 0; b < B; ++b) max_pos = pos[b] > max_pos ? pos[b] : max_pos;
-  // three or more overlapping stages: other stages' kernels share the GPU
-  const bool shared = m->N >= 3 && !m->single && m->overlap;
-  const int chunk = attn_chunk(hd, nkv, B, max_pos, m->num_sms, shared);
+  const int chunk = attn_chunk(hd, nkv, B, max_pos, m->num_sms);
   // Programmatic dependent launch chains the kernels inside a stage walk; the
   // first kernel of each walk follows cross-stream event waits and is launched
   // with full stream ordering instead.
