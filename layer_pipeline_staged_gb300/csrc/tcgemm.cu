@@ -7,9 +7,11 @@
 // micro-chunk of rows at a time).
 //
 // Operands:
-//   - A = the packed weights W [R][K] bf16, row-major (the batch-1 layout, so
-//     no second copy of any matrix), 128-row x 64-column tiles by 2D TMA with
-//     the 128-byte swizzle, which is the canonical K-major layout the MMA reads;
+//   - A = the packed weights W [R][K], row-major (the batch-1 layout, so no
+//     second copy of any matrix), 128-row x 64-column tiles by 2D TMA: bf16
+//     with the 128-byte swizzle, which is the canonical K-major layout the MMA
+//     reads; int8 unswizzled, widened to that bf16 layout by four warps (int8
+//     values are exact in bf16; the per-row scale multiplies the result);
 //   - B = the activations as two bf16 planes, X = hi + lo with hi = bf16(x) and
 //     lo = bf16(x - hi): rows [0, NP) hold hi, rows [NP, 2 NP) lo, so every
 //     activation keeps about 16 significant bits. The two planes are one
@@ -32,10 +34,11 @@
 // of the first stages before the programmatic-dependent-launch wait, as they
 // never depend on the previous kernel); warp 1 allocates TMEM and its lane 0
 // issues the MMAs and the tcgen05.commit arrivals that free ring stages and
-// publish finished accumulators; warps 2..9 (two per 32-lane TMEM quarter,
-// each taking half of the token columns) read the accumulators with
-// tcgen05.ld and apply the epilogue. Every wait is
-// bounded and reports through the status word instead of hanging.
+// publish finished accumulators, and before the CTA ends waits for its own
+// MMAs to complete; warps 2..9 (two per 32-lane TMEM quarter, each taking
+// half of the token columns) read the accumulators with tcgen05.ld and apply
+// the epilogue; warps 10..13 widen int8 weight tiles. Every wait is bounded
+// and reports through the status word instead of hanging.
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tc.cuh"
