@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--persistent", action="store_true",
                     help="batch 1: the persistent stage kernel (one launch per stage and step) instead of "
                          "the default chained per-projection kernels")
+    ap.add_argument("--graph", action="store_true",
+                    help="every step replays as one CUDA graph (LPS_FLAG_GRAPH)")
     ap.add_argument("--repeats", type=int, default=None,
                     help="extra timed passes of the same K steps for a median (default: about 2 s worth)")
     return ap.parse_args()
@@ -300,7 +302,7 @@ def main():
                 weight_dtype=1 if cfg.weight_dtype == "int8" else 0, kv_dtype=0, max_ctx=max_ctx,
                 batch=cfg.batch, pending_depth=4, rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps,
                 flags=(lps.LPS_FLAG_SERIAL_STEPS if args.serial else 0) | (lps.LPS_FLAG_VERIFY if M else 0)
-                | (lps.LPS_FLAG_PERSISTENT if args.persistent else 0))
+                | (lps.LPS_FLAG_PERSISTENT if args.persistent else 0) | (lps.LPS_FLAG_GRAPH if args.graph else 0))
     plan = lps.stage_plan_create(cfg.n_layers, cuts=list(cfg.cuts))
     model = lps.model_bind(plan, desc, w, device=local)
     B, V = cfg.batch, cfg.vocab
@@ -458,7 +460,8 @@ def main():
     peaks, peak_src = measured_peaks()
     dom_bytes = per_launch[dom]
     dom_avg_s = dom_ms / 1e3 / max(dom_n, 1)
-    achieved = dom_bytes / dom_avg_s / 1e9
+    # (graph steps run no per-kernel timers: no live launch time then)
+    achieved = dom_bytes / dom_avg_s / 1e9 if dom_n else None
     wl = workload_name(cfg, ctx, K)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -479,7 +482,8 @@ def main():
         "bytes_per_step": sum(step_bytes) / K,
         "value_arm": "decode_step_device: token ids and logits resident in HBM, K steps enqueued back to back "
                      "(no host copies; the deferred host readback is timed in e2e)",
-        "path": "persistent stage kernel" if persistent else "chained per-projection kernels",
+        "path": ("persistent stage kernel" if persistent else "chained per-projection kernels")
+                + (", one CUDA graph per step" if args.graph else ""),
         "repeats": {"passes": len(rep_ms), "steps_per_pass": K, "ms_per_step_median": statistics.median(rep_ms),
                     "ms_per_step_min": min(rep_ms), "ms_per_step_max": max(rep_ms),
                     "tokens_per_s_median": job_rate(world, B, 1, statistics.median(rep_ms) / 1e3)},
@@ -487,7 +491,7 @@ def main():
                                "of step bytes; launches timed live" + ("" if persistent else
                                                                          ", stages serialized") + ")",
                      "bound": "hbm",
-                     "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"] if achieved else None,
                      "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
                      else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_us": dom_avg_s * 1e6,

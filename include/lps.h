@@ -125,6 +125,17 @@ int stage_plan_solve(int n_layers, int n_stages, const uint64_t* layer_bytes, co
                                       the default chain, so it is opt-in. Ignored (stats.persistent = 0)
                                       for batch > 1, verify rows, the single-stream arm and shapes
                                       the kernel does not take. */
+#define LPS_FLAG_GRAPH 32u          /* every step replays as one CUDA graph (ninfer pipeline-stages.md,
+                                      "StageLink": decode captures the whole pass into one graph):
+                                      the step is captured from stage 0's stream, the other stages'
+                                      streams fork from it and join back through the boundary
+                                      events, and each step's capture updates the instantiated graph
+                                      in place (positions, logits buffer and attention grid change)
+                                      before it is launched. Same bits as the stream path. Graph
+                                      steps run one after another (the next replay starts when the
+                                      previous one has ended), so consecutive steps do not overlap
+                                      as they do on the streams; the per-kernel timers do not time
+                                      graph steps. Not with LPS_FLAG_PERSISTENT (LPS_EINVAL). */
 #define LPS_FLAG_SERIAL_STEPS 4u   /* make stage 0 of step t+1 also wait for the last stage of step t.
                                       By default stages of consecutive steps overlap, bounded
                                       only by the slot events (tokens t+1.. keep running while

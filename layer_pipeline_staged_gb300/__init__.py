@@ -20,7 +20,7 @@ import numpy as np
 
 from . import _capi
 from ._capi import (KERNELS, LPS_EBUSY, LPS_ECUDA, LPS_EINVAL, LPS_ENOMEM, LPS_ETIMEDOUT,  # noqa: F401
-                    LPS_FLAG_KEEP_ATTN_OUT, LPS_FLAG_SERIAL_STEPS, LPS_FLAG_SINGLE_STREAM, LPS_FLAG_VERIFY, LPS_FLAG_PERSISTENT,
+                    LPS_FLAG_KEEP_ATTN_OUT, LPS_FLAG_SERIAL_STEPS, LPS_FLAG_SINGLE_STREAM, LPS_FLAG_VERIFY, LPS_FLAG_PERSISTENT, LPS_FLAG_GRAPH,
                     LPS_NOALLOC_SCRATCH_BYTES,
                     LPS_OK)
 

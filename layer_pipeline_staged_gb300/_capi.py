@@ -23,6 +23,7 @@ LPS_FLAG_KEEP_ATTN_OUT = 2
 LPS_FLAG_SERIAL_STEPS = 4
 LPS_FLAG_VERIFY = 8
 LPS_FLAG_PERSISTENT = 16
+LPS_FLAG_GRAPH = 32
 
 KERNELS = {"qkv": 0, "attn": 1, "oproj": 2, "gateup": 3, "down": 4, "head": 5, "embed": 6, "stage": 7, "merge": 8,
            "pf_split": 9, "pf_gemm": 10, "pf_attn": 11, "pf_merge": 12}

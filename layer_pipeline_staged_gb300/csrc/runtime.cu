@@ -270,6 +270,12 @@ struct lps_model {
   bool skinny = false;  // batch > 1: tensor-core skinny GEMMs on the tiled weight layout
   bool verify = false;  // LPS_FLAG_VERIFY: the batch rows are consecutive positions of one sequence
   bool persist = false; // batch 1: one persistent stage kernel per stage and step, all on one stream
+  bool graph = false;   // LPS_FLAG_GRAPH: every step replays as one CUDA graph
+  bool capturing = false;  // a step is being captured: no cross-step waits, no timers
+  cudaGraphExec_t gexec = nullptr;
+  std::vector<cudaEvent_t> gjoin;  // per stage: its stream's work so far, for the graph's fork and join
+  cudaEvent_t gdone = nullptr;     // the graph launch, for the stage streams' later work
+  uint64_t graph_instantiations = 0;
   StageKernelPlan skp{};
   lps_alloc_fn alloc = nullptr;
   lps_free_fn free_fn = nullptr;
@@ -372,6 +378,10 @@ void release(lps_model* m) {
   for (auto& p : m->pend)
     if (p.ev_done) cudaEventDestroy(p.ev_done);
   if (m->ev_step) cudaEventDestroy(m->ev_step);
+  for (cudaEvent_t e : m->gjoin)
+    if (e) cudaEventDestroy(e);
+  if (m->gdone) cudaEventDestroy(m->gdone);
+  if (m->gexec) cudaGraphExecDestroy(m->gexec);
   for (auto& t : m->timers)
     for (auto& e : t.ev) {
       cudaEventDestroy(e.first);
@@ -595,7 +605,7 @@ unsigned long long* trace_block(lps_model* m, int n) {
 int timer_begin(lps_model* m, int kind, cudaStream_t s, cudaEvent_t* stop) {
   *stop = nullptr;
   KTimer& t = m->timers[kind];
-  if (!t.on) return 0;
+  if (!t.on || m->capturing) return 0;
   if (t.used == t.ev.size()) {
     cudaEvent_t a, b;
     if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) return -1;
@@ -741,6 +751,9 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
   // batch 1, on request: the persistent stage kernel where its shapes fit
   m->skp = stage_kernel_plan(E, nq, nkv, hd, d.ffn, d.vocab, int8, m->num_sms, max_smem);
   m->persist = B == 1 && !m->verify && !m->single && (d.flags & LPS_FLAG_PERSISTENT) && m->skp.ok;
+  m->graph = (d.flags & LPS_FLAG_GRAPH) != 0;
+  if (m->graph && (d.flags & LPS_FLAG_PERSISTENT)) return bail(LPS_EINVAL, "LPS_FLAG_GRAPH replays the chained kernels; "
+                                                                             "it does not combine with LPS_FLAG_PERSISTENT");
 
   // rope table (cos, sin) of angle pos * theta^(-2i/hd), computed in double
   std::vector<float2> rope(static_cast<size_t>(d.max_ctx) * half);
@@ -802,8 +815,9 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
     // the bits do not change. Measured on the 8B bf16 step (4 stages, context
     // 8192): 2.872 ms with every projection on all 152 SMs, 2.726 with these on
     // 76 (114: 2.752; 57: 2.776; gate/up on fewer SMs as well: slower); with 2
-    // stages (8B int8) 2% slower, so not there.
-    const int shared_sms = (N >= 3 && !m->single && m->overlap) ? m->num_sms / 2 : m->num_sms;
+    // stages (8B int8) 2% slower, so not there. Graph steps replay one after
+    // another (no other step's stages run beside them): full grids there.
+    const int shared_sms = (N >= 3 && !m->single && m->overlap && !m->graph) ? m->num_sms / 2 : m->num_sms;
     S.plan_qkv = gemv_plan(rows_qkv, E, 2, int8, shared_sms, max_smem);
     S.plan_o = gemv_plan(E, qw, 1, int8, shared_sms, max_smem);
     S.plan_gu = gemv_plan(2 * d.ffn, E, 2, int8, m->num_sms, max_smem);
@@ -967,6 +981,14 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
 
   if (cudaEventCreateWithFlags(&m->ev_step, cudaEventDisableTiming) != cudaSuccess)
     return bail(LPS_ECUDA, "cudaEventCreate failed");
+  if (m->graph) {
+    m->gjoin.assign(N, nullptr);
+    for (auto& e : m->gjoin)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+        return bail(LPS_ECUDA, "cudaEventCreate failed");
+    if (cudaEventCreateWithFlags(&m->gdone, cudaEventDisableTiming) != cudaSuccess)
+      return bail(LPS_ECUDA, "cudaEventCreate failed");
+  }
 
   // logits: one eager buffer and the deferred-readback ring
   const size_t logits_bytes = sizeof(float) * B * static_cast<size_t>(d.vocab);
@@ -1141,10 +1163,9 @@ int enqueue_persistent(lps_model* m, const int32_t* tok_host, const int32_t* tok
   return LPS_OK;
 }
 
-// Enqueue one step; the last stage writes logits_dev [B][V].
-int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, const int32_t* pos, float* logits_dev,
-                 const char* FN) {
-  if (m->persist) return enqueue_persistent(m, tok_host, tok_dev, pos, logits_dev, FN);
+// Enqueue one step's kernels on the stage streams; the last stage writes logits_dev [B][V].
+int enqueue_step_streams(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, const int32_t* pos,
+                         float* logits_dev, const char* FN) {
   const lps_model_desc& d = m->d;
   const int N = m->N, B = d.batch, E = d.n_embd, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads;
   const int qw = nq * hd, half = hd / 2;
@@ -1182,8 +1203,11 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
     layer_trace = -1;
     if (!m->single) {
       if (s > 0) CK(cudaStreamWaitEvent(cs, m->bd[s - 1].ev_tx[par], 0), "wait ev_tx");
-      if (s + 1 < N) CK(cudaStreamWaitEvent(cs, m->bd[s].ev_rx[par], 0), "wait ev_rx");
-      if (s == 0 && N > 1 && !m->overlap) CK(cudaStreamWaitEvent(cs, m->ev_step, 0), "wait previous step");
+      // (a captured step replays only after the previous graph launch has
+      // completed, so it waits for no earlier step)
+      if (s + 1 < N && !m->capturing) CK(cudaStreamWaitEvent(cs, m->bd[s].ev_rx[par], 0), "wait ev_rx");
+      if (s == 0 && N > 1 && !m->overlap && !m->capturing)
+        CK(cudaStreamWaitEvent(cs, m->ev_step, 0), "wait previous step");
     } else if (s > 0) {
       CK(cudaMemcpyAsync(S.h, m->bd[s - 1].slot[par], sizeof(float) * B * E, cudaMemcpyDeviceToDevice, cs),
          "boundary copy");
@@ -1325,7 +1349,8 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
         p.wait_limit = m->wait_limit;
         LAUNCH(LPS_KERNEL_OPROJ, cs, p, launch_gemv(p, kEpiResidual, false, m->int8, S.plan_o, cs, pdl));
       }
-      if (first && s > 0 && !m->single) CK(cudaEventRecord(m->bd[s - 1].ev_rx[par], cs), "record ev_rx");
+      if (first && s > 0 && !m->single && !m->capturing)
+        CK(cudaEventRecord(m->bd[s - 1].ev_rx[par], cs), "record ev_rx");
       // RMSNorm -> gate/up -> SwiGLU
       if (m->skinny) {
         SkinnyParams p = skinny_params(m, L.w_gu, L.s_gu, 2 * d.ffn, E, pos);
@@ -1424,7 +1449,7 @@ int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, 
       p.wait_limit = m->wait_limit;
       LAUNCH(LPS_KERNEL_HEAD, cs, p, launch_gemv(p, kEpiStore, true, m->int8, S.plan_head, cs, pdl));
     }
-    if (N > 1 && !m->single && !m->overlap) CK(cudaEventRecord(m->ev_step, cs), "record step event");
+    if (N > 1 && !m->single && !m->overlap && !m->capturing) CK(cudaEventRecord(m->ev_step, cs), "record step event");
   }
 #undef LAUNCH
   if (m->verify)
@@ -1683,6 +1708,83 @@ int enqueue_prefill_chunk(lps_model* m, int seq, int pos0, int ntok, int tok_off
   ++P.chunks;
   m->stats.kernel_launches += launches;
   return LPS_OK;
+}
+
+// One step as a CUDA graph (the pages' decode captures the whole pass into one
+// graph: ninfer pipeline-stages.md, "StageLink"). The step is captured from
+// stage 0's stream -- the other stages' streams join through the ev_tx events
+// and are joined back at the end -- and the captured graph updates the
+// instantiated one in place (cudaGraphExecUpdate: the positions, the logits
+// buffer and the attention's grid change from step to step; a fresh
+// instantiation when the topology changes), which is then launched on stage
+// 0's stream. Every replay runs after the previous one, so the captured step
+// drops the waits on earlier steps' events: graph steps do not overlap one
+// another, only the stages inside a step do.
+int enqueue_step_graph(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, const int32_t* pos,
+                       float* logits_dev, const char* FN) {
+  const int N = m->N;
+  const cudaStream_t s0 = m->stream(0);
+  // the replay follows everything already enqueued on any stage's stream
+  for (int s = 1; s < N; ++s) {
+    if (m->stream(s) == s0) continue;
+    CK(cudaEventRecord(m->gjoin[s], m->stream(s)), "record join event");
+    CK(cudaStreamWaitEvent(s0, m->gjoin[s], 0), "wait join event");
+  }
+  CK(cudaStreamBeginCapture(s0, cudaStreamCaptureModeRelaxed), "cudaStreamBeginCapture");
+  m->capturing = true;
+  int rc = enqueue_step_streams(m, tok_host, tok_dev, pos, logits_dev, FN);
+  cudaError_t e = cudaSuccess;
+  for (int s = 1; s < N && rc == LPS_OK && e == cudaSuccess; ++s) {
+    if (m->stream(s) == s0) continue;
+    e = cudaEventRecord(m->gjoin[s], m->stream(s));
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s0, m->gjoin[s], 0);
+  }
+  cudaGraph_t g = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(s0, &g);
+  m->capturing = false;
+  if (rc != LPS_OK || e != cudaSuccess || ec != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    m->failed = true;
+    if (rc != LPS_OK) return rc;
+    return cuda_fail(FN, "step capture", e != cudaSuccess ? e : ec);
+  }
+  if (m->gexec) {
+    cudaGraphExecUpdateResultInfo info;
+    if (cudaGraphExecUpdate(m->gexec, g, &info) != cudaSuccess) {
+      cudaGetLastError();
+      cudaGraphExecDestroy(m->gexec);
+      m->gexec = nullptr;
+    }
+  }
+  if (!m->gexec) {
+    e = cudaGraphInstantiate(&m->gexec, g, 0);
+    if (e != cudaSuccess) {
+      cudaGraphDestroy(g);
+      m->gexec = nullptr;
+      m->failed = true;
+      return cuda_fail(FN, "graph instantiation", e);
+    }
+    ++m->graph_instantiations;
+  }
+  cudaGraphDestroy(g);
+  e = cudaGraphLaunch(m->gexec, s0);
+  if (e != cudaSuccess) {
+    m->failed = true;
+    return cuda_fail(FN, "graph launch", e);
+  }
+  // whatever follows on a stage's stream (readback, events, prefill) follows the replay
+  CK(cudaEventRecord(m->gdone, s0), "record graph event");
+  for (int s = 1; s < N; ++s)
+    if (m->stream(s) != s0) CK(cudaStreamWaitEvent(m->stream(s), m->gdone, 0), "wait graph event");
+  return LPS_OK;
+}
+
+// Enqueue one step; the last stage writes logits_dev [B][V].
+int enqueue_step(lps_model* m, const int32_t* tok_host, const int32_t* tok_dev, const int32_t* pos, float* logits_dev,
+                 const char* FN) {
+  if (m->persist) return enqueue_persistent(m, tok_host, tok_dev, pos, logits_dev, FN);
+  if (m->graph) return enqueue_step_graph(m, tok_host, tok_dev, pos, logits_dev, FN);
+  return enqueue_step_streams(m, tok_host, tok_dev, pos, logits_dev, FN);
 }
 
 int read_status(lps_model* m, const int* status, const char* FN) {
