@@ -223,7 +223,11 @@ typedef struct lps_runtime {
  *   plan  a stage plan whose n_layers equals desc->n_layers (not retained);
  *   rt    optional runtime hooks, or NULL (device 0, cudaMalloc, own streams).
  * LPS_EINVAL for unsupported shapes, LPS_ENOMEM / LPS_ECUDA on device failure
- * (everything allocated so far is released). */
+ * (everything allocated so far is released). The descriptor, the weight
+ * pointers and the runtime hooks are checked before the device is touched:
+ * those refusals (LPS_EINVAL) come the same with or without a GPU; the
+ * limits that depend on the device (shared memory per block, SM count for
+ * batch > 1) are checked after. */
 int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc, const lps_model_weights* w,
                const lps_runtime* rt, lps_model** out);
 

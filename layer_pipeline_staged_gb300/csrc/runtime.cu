@@ -504,7 +504,7 @@ bool place_matrix(lps_model* m, Uploader& up, int rows, int K, RowPtr row_ptr, R
   return up.err == cudaSuccess;
 }
 
-bool check_matrix(const lps_model* m, const lps_matrix& x) { return x.w && (!m->int8 || x.scale); }
+bool check_matrix(bool int8, const lps_matrix& x) { return x.w && (!int8 || x.scale); }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -640,10 +640,29 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
   if (d.n_embd < 1 || d.n_q_heads < 1 || d.n_kv_heads < 1 || d.ffn < 1 || d.vocab < 1 || d.max_ctx < 1)
     return fail(LPS_EINVAL, FN, "shape fields must be positive");
   if (d.batch < 1 || d.batch > kMaxBatch) return fail(LPS_EINVAL, FN, "batch must be in 1..8");
+  if ((d.flags & LPS_FLAG_GRAPH) && (d.flags & LPS_FLAG_PERSISTENT))
+    return fail(LPS_EINVAL, FN, "LPS_FLAG_GRAPH replays the chained kernels; it does not combine with LPS_FLAG_PERSISTENT");
   if (d.n_q_heads % d.n_kv_heads) return fail(LPS_EINVAL, FN, "n_q_heads must be a multiple of n_kv_heads");
   if (!attn_supported(d.head_dim, d.n_q_heads / d.n_kv_heads))
     return fail(LPS_EINVAL, FN, "head_dim must be 64 or 128 and n_q_heads/n_kv_heads in {1,2,4,8}");
+  if (d.n_embd % 4) return fail(LPS_EINVAL, FN, "n_embd must be a multiple of 4");
+  if (!(d.rms_eps > 0.f) || !(d.rope_theta > 0.f)) return fail(LPS_EINVAL, FN, "rms_eps and rope_theta must be > 0");
+  // the attention addresses a layer's cache rows with 32-bit TMA coordinates
+  if (static_cast<long long>(d.batch) * d.n_kv_heads * d.max_ctx > 0x7fffffffll)
+    return fail(LPS_EINVAL, FN, "batch * n_kv_heads * max_ctx must stay below 2^31 cache rows per layer");
+  if (!w->layers || !w->out_norm || !w->embed.w || !w->lm_head.w) return fail(LPS_EINVAL, FN, "missing weights");
   const bool int8 = d.weight_dtype == LPS_WEIGHT_INT8_ROWSCALE;
+  for (int l = 0; l < d.n_layers; ++l) {
+    const lps_layer_weights& L = w->layers[l];
+    if (!L.attn_norm || !L.ffn_norm || !check_matrix(int8, L.wq) || !check_matrix(int8, L.wk) ||
+        !check_matrix(int8, L.wv) || !check_matrix(int8, L.wo) || !check_matrix(int8, L.w_gate) ||
+        !check_matrix(int8, L.w_up) || !check_matrix(int8, L.w_down))
+      return fail(LPS_EINVAL, FN, "layer " + std::to_string(l) + " has a missing tensor or scale");
+  }
+  if (!check_matrix(int8, w->embed) || !check_matrix(int8, w->lm_head))
+    return fail(LPS_EINVAL, FN, "embed or lm_head is missing its row scales");
+  if (rt && rt->alloc && !rt->free) return fail(LPS_EINVAL, FN, "rt->free is required with rt->alloc");
+  // (every check above reads the arguments only; the ones below ask the device)
   const int qw = d.n_q_heads * d.head_dim;
   const int dev = rt ? rt->device : 0;
   int max_smem = 0;
@@ -655,7 +674,6 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
       !gemv_supported(d.ffn, 1, int8, max_smem))
     return fail(LPS_EINVAL, FN, "n_embd, n_q_heads*head_dim and ffn need whole 16-byte weight rows, and two "
                                 "rows (row pairs) plus the fp32 input vector must fit in shared memory");
-  if (d.n_embd % 4) return fail(LPS_EINVAL, FN, "n_embd must be a multiple of 4");
   if (d.batch > 1) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
@@ -671,11 +689,6 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
       return fail(LPS_EINVAL, FN, "batch > 1 needs every projection's columns in multiples of 16, rows even and "
                                   "at most 64 16-row units (1024 rows) per SM");
   }
-  if (!(d.rms_eps > 0.f) || !(d.rope_theta > 0.f)) return fail(LPS_EINVAL, FN, "rms_eps and rope_theta must be > 0");
-  // the attention addresses a layer's cache rows with 32-bit TMA coordinates
-  if (static_cast<long long>(d.batch) * d.n_kv_heads * d.max_ctx > 0x7fffffffll)
-    return fail(LPS_EINVAL, FN, "batch * n_kv_heads * max_ctx must stay below 2^31 cache rows per layer");
-  if (!w->layers || !w->out_norm || !w->embed.w || !w->lm_head.w) return fail(LPS_EINVAL, FN, "missing weights");
 
   lps_model* m = new lps_model();
   m->d = d;
@@ -685,27 +698,10 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
   m->fence = plan->fence;
   m->N = static_cast<int>(plan->fence.size()) - 1;
   m->device = rt ? rt->device : 0;
-  if (rt && rt->alloc && !rt->free) {
-    delete m;
-    return fail(LPS_EINVAL, FN, "rt->free is required with rt->alloc");
-  }
   if (rt) {
     m->alloc = rt->alloc;
     m->free_fn = rt->free;
     m->alloc_ctx = rt->alloc_ctx;
-  }
-  for (int l = 0; l < d.n_layers; ++l) {
-    const lps_layer_weights& L = w->layers[l];
-    if (!L.attn_norm || !L.ffn_norm || !check_matrix(m, L.wq) || !check_matrix(m, L.wk) || !check_matrix(m, L.wv) ||
-        !check_matrix(m, L.wo) || !check_matrix(m, L.w_gate) || !check_matrix(m, L.w_up) ||
-        !check_matrix(m, L.w_down)) {
-      delete m;
-      return fail(LPS_EINVAL, FN, "layer " + std::to_string(l) + " has a missing tensor or scale");
-    }
-  }
-  if (!check_matrix(m, w->embed) || !check_matrix(m, w->lm_head)) {
-    delete m;
-    return fail(LPS_EINVAL, FN, "embed or lm_head is missing its row scales");
   }
 
   auto bail = [&](int code, const std::string& why) {
@@ -752,8 +748,6 @@ extern "C" int model_bind(const lps_stage_plan* plan, const lps_model_desc* desc
   m->skp = stage_kernel_plan(E, nq, nkv, hd, d.ffn, d.vocab, int8, m->num_sms, max_smem);
   m->persist = B == 1 && !m->verify && !m->single && (d.flags & LPS_FLAG_PERSISTENT) && m->skp.ok;
   m->graph = (d.flags & LPS_FLAG_GRAPH) != 0;
-  if (m->graph && (d.flags & LPS_FLAG_PERSISTENT)) return bail(LPS_EINVAL, "LPS_FLAG_GRAPH replays the chained kernels; "
-                                                                             "it does not combine with LPS_FLAG_PERSISTENT");
 
   // rope table (cos, sin) of angle pos * theta^(-2i/hd), computed in double
   std::vector<float2> rope(static_cast<size_t>(d.max_ctx) * half);
