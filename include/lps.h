@@ -194,8 +194,14 @@ typedef struct lps_model_weights {
  * embedding; last_stage_bytes = the LM head, final norm and logits buffers;
  * every_stage_bytes = a stage's activations, attention partials (one per 64
  * positions, a bound), RoPE table and boundary slots at desc->max_ctx -- a
- * close estimate, not the exact allocation. Host arrays of n_layers entries.
- * LPS_EINVAL for NULL arguments or a bad shape. */
+ * close estimate, not the exact allocation. Not counted: the chunked
+ * prefill's workspace, allocated per stage at the first model_prefill call
+ * (rows of 128 tokens: hidden, q and activation planes, the chunk
+ * attention's partials over about 2 x SMs / n_kv_heads key chunks, the
+ * GEMM's per-CTA partial tiles; about 120 MB per stage at the 8B shape on
+ * 152 SMs); it depends on the device's SM count, which this host-only call
+ * does not know. Host arrays of n_layers entries. LPS_EINVAL for NULL
+ * arguments or a bad shape. */
 int model_stage_bytes(const lps_model_desc* desc, uint64_t* layer_bytes, uint64_t* layer_unit_bytes,
                       uint64_t* first_stage_bytes, uint64_t* last_stage_bytes, uint64_t* every_stage_bytes);
 
