@@ -76,6 +76,23 @@ def workload_name(cfg, ctx, steps, readback="deferred"):
             f"{len(cfg.fence) - 1} stages (cuts {','.join(map(str, cfg.cuts))}), {readback} readback")
 
 
+def resolve_fill(fill: str, batch: int, verify_rows: int) -> str:
+    """How the context rows before the timed steps are written (auto: the chunked prefill
+    where the model takes it, i.e. batch 1 without verify rows, else synthetic rows)."""
+    if fill == "auto":
+        return "prefill" if (batch == 1 and not verify_rows) else "synthetic"
+    return fill
+
+
+def arm_config(cfg, ctx: int, steps: int, n_stages: int, n_replicas: int, fill: str, overlap: bool) -> dict:
+    """The line's `config`, the same for the GPU arm and the reference arm."""
+    return {"workload": workload_name(cfg, ctx, steps),
+            "l2": "inputs larger than L2 (every step streams all weights from HBM)",
+            "cache_fill": fill, "steps_overlap": overlap,
+            "parallelism": f"{n_stages} stages on one device"
+            + (f", {n_replicas} independent replicas" if n_replicas > 1 else "")}
+
+
 def dtype_of(cfg):
     return "int8" if cfg.weight_dtype == "int8" else "bf16"
 
@@ -249,10 +266,12 @@ def run_reference(args, cfg, ctx):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / n, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": dtype_of(cfg), "data": "synthetic",
-            "config": {"workload": workload_name(cfg, ctx, args.steps), "parallelism": "stages on one device"},
+            "config": arm_config(cfg, ctx, args.steps, len(cfg.fence) - 1, args.gpus,
+                                 resolve_fill(args.fill, cfg.batch, args.verify), not args.serial),
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": orc.L.orc_get_threads(), "kind": "oracle",
-                             "sample": f"{n} of {args.steps} decode steps at positions {pos0}..{pos0 + n - 1}, "
-                                       f"cache filled synthetically (weights drawn in {gen_s:.0f} s, untimed)"},
+                             "sample": f"{n} of {args.steps} decode steps at positions {pos0}..{pos0 + n - 1}; "
+                                       f"the oracle's cache rows before them are zeros (their values do not "
+                                       f"change a step's time; weights drawn in {gen_s:.0f} s, untimed)"},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -311,9 +330,7 @@ def main():
     seqs = 1 if M else B  # sequences with a cache of their own
     # context rows [0, start): the chunked prefill of a seeded prompt, synthetic
     # cache contents, or teacher-forced decode steps
-    fill = args.fill
-    if fill == "auto":
-        fill = "prefill" if (B == 1 and not M) else "synthetic"
+    fill = resolve_fill(args.fill, B, M)
     prefill_info = None
     if fill == "prefill" and start > 0:
         ptoks = synth.make_tokens(cfg, start, seed=cfg.seed_t + 9)
@@ -462,7 +479,6 @@ def main():
     dom_avg_s = dom_ms / 1e3 / max(dom_n, 1)
     # (graph steps run no per-kernel timers: no live launch time then)
     achieved = dom_bytes / dom_avg_s / 1e9 if dom_n else None
-    wl = workload_name(cfg, ctx, K)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg, w, ctx, args.cpu_seconds)
@@ -473,10 +489,7 @@ def main():
         "value": tok_s, "unit": "tokens/s", "n_gpus": n, "steps": K, "warmup": W,
         "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": dtype_of(cfg), "data": "synthetic",
-        "config": {"workload": wl, "l2": "inputs larger than L2 (every step streams all weights from HBM)",
-                   "cache_fill": fill, "steps_overlap": not args.serial,
-                   "parallelism": f"{plan.n_stages} stages on one device"
-                   + (f", {n} independent replicas" if n > 1 else "")},
+        "config": arm_config(cfg, ctx, K, plan.n_stages, n, fill, not args.serial),
         "hbm_gbs": hbm_gbs, "hbm_frac_of_8tbs": hbm_gbs / NOMINAL_HBM_GBS,
         "hbm_frac_of_measured": hbm_gbs / peaks["hbm_gbs"],
         "bytes_per_step": sum(step_bytes) / K,

@@ -25,3 +25,18 @@ def test_reference_arm_json_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    # the same config dict the GPU arm prints for these arguments (batch 1: the context by prefill)
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    cfg = synth.CONFIGS["tiny"]
+    assert d["config"] == bench.arm_config(cfg, cfg.ctx, 2, len(cfg.fence) - 1, 1, "prefill", True)
+
+
+def test_fill_resolution():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.resolve_fill("auto", 1, 0) == "prefill"
+    assert bench.resolve_fill("auto", 8, 0) == "synthetic"
+    assert bench.resolve_fill("auto", 8, 8) == "synthetic"  # verify rows: batch = rows of one sequence
+    assert bench.resolve_fill("decode", 1, 0) == "decode"
