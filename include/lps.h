@@ -60,15 +60,18 @@ typedef struct lps_pending lps_pending;
 int stage_plan_create(int n_layers, const int* cuts, int n_cuts, lps_stage_plan** out);
 
 /* The same plan spelled as layer counts per stage (ninfer pipeline-stages.md,
- * "How it works": `--stage-layers 30,34`). counts: host int[n_stages], each >= 1. */
+ * "How it works": `--stage-layers 30,34`). counts: host int[n_stages], each >= 1.
+ * LPS_EINVAL for NULL counts or out, n_stages < 1 or a count < 1. */
 int stage_plan_from_counts(const int* counts, int n_stages, lps_stage_plan** out);
 
+/* Free a plan (models bound from it keep their own copy). NULL is a no-op. */
 void stage_plan_destroy(lps_stage_plan* plan);
 
-/* Number of stages N (>= 1). */
+/* Number of stages N (>= 1); LPS_EINVAL for NULL. */
 int stage_plan_n_stages(const lps_stage_plan* plan);
 
-/* Copy the fence (N+1 ints) into host fence[cap]; returns N+1, or LPS_EINVAL if cap < N+1. */
+/* Copy the fence (N+1 ints) into host fence[cap]; returns N+1, or LPS_EINVAL for
+ * NULL arguments or cap < N+1. */
 int stage_plan_fence(const lps_stage_plan* plan, int* fence, int cap);
 
 /* The stage that owns layer il (memra_engine::pp, stage_of); LPS_EINVAL if il is out of range. */
@@ -248,7 +251,10 @@ void model_destroy(lps_model* m);
  * and copies the logits to host logits[B][vocab] (fp32, caller-owned) before
  * returning. Requires 0 <= tokens[b] < vocab and 0 <= pos[b] <= filled[b]
  * (the rows written so far; rewinding is allowed, holes are not) and
- * pos[b] < max_ctx; afterwards filled[b] = pos[b] + 1. */
+ * pos[b] < max_ctx; afterwards filled[b] = pos[b] + 1. LPS_EINVAL when an
+ * argument breaks these rules (nothing is enqueued); LPS_ECUDA when a CUDA
+ * call fails or a kernel reports a device-side error (the model is then
+ * unusable: every later step or prefill on it returns LPS_ECUDA). */
 int decode_step(lps_model* m, const int32_t* tokens, const int32_t* pos, float* logits);
 
 /* The same step, ending without the logits copy (memra_engine::pp,
@@ -263,14 +269,17 @@ int decode_step_deferred(lps_model* m, const int32_t* tokens, const int32_t* pos
  * LPS_ETIMEDOUT leaves the handle valid. A handle may be waited more than once. */
 int pending_wait(lps_pending* p, float* logits, int timeout_ms);
 
-/* Release a pending handle, waited or not (dropping without waiting is safe). */
+/* Release a pending handle, waited or not (dropping without waiting is safe);
+ * its readback slot is free again. NULL is a no-op. */
 void pending_free(lps_pending* p);
 
 /* The step with device-resident input and output: tokens is a device int[B],
  * pos a host int[B] (the per-step position snapshot), logits a device
  * float[B][vocab]. Returns once the step is enqueued; the logits are ready
  * when model_synchronize returns or after work ordered on the stream that
- * model_stream(m, N-1) returns. */
+ * model_stream(m, N-1) returns. The same refusals as decode_step, except that
+ * the token ids, being on the device, are not range-checked here: each must be
+ * in [0, vocab). */
 int decode_step_device(lps_model* m, const int32_t* tokens, const int32_t* pos, float* logits);
 
 /* ---- chunked prefill through the stages -------------------------------- */
@@ -315,7 +324,8 @@ int model_set_wait_limit(lps_model* m, long long cycles);
  * kernel family without other stages' kernels running beside it. */
 int model_set_serial_steps(lps_model* m, int serial);
 
-/* The cudaStream_t of stage s (0..N-1) or of the readback stream (s = N). */
+/* The cudaStream_t of stage s (0..N-1) or of the readback stream (s = N), into
+ * *stream. LPS_EINVAL for NULL arguments or s outside 0..N. */
 int model_stream(const lps_model* m, int s, void** stream);
 
 /* ---- errors, counters, test hooks ---------------------------------------- */
@@ -336,24 +346,30 @@ typedef struct lps_stats {
                                   0: the chained per-projection kernels (the default) */
 } lps_stats;
 
+/* Copy the counters into *out (host). LPS_EINVAL for NULL arguments. */
 int model_stats(const lps_model* m, lps_stats* out);
 
 /* Copy the cache rows of (layer, sequence b) out of or into the device:
  * host buffer [2][nkv][max_ctx][hd] bf16 (K then V), bytes must equal
  * 4 * nkv * max_ctx * hd. Import also sets filled[b] = filled (0..max_ctx).
- * Both synchronize the owning stage's stream. */
+ * Both synchronize the owning stage's stream. With LPS_FLAG_VERIFY only b = 0
+ * exists. LPS_EINVAL for a NULL model or buffer, a layer or sequence out of
+ * range, another byte count, or (import) filled outside 0..max_ctx. */
 int model_kv_export(const lps_model* m, int layer, int b, void* host, size_t bytes);
 int model_kv_import(lps_model* m, int layer, int b, const void* host, size_t bytes, int filled);
 
 /* Attention output of (layer, sequence b) in the latest step, host float[nq*hd];
- * needs LPS_FLAG_KEEP_ATTN_OUT. */
+ * synchronizes the layer's stage. LPS_EINVAL for bad arguments or a model bound
+ * without LPS_FLAG_KEEP_ATTN_OUT. */
 int model_attn_out(const lps_model* m, int layer, int b, float* host);
 
 /* Per-kernel timing with CUDA events on the launching stream, for the kernel
  * family `kind` (LPS_KERNEL_QKV .. LPS_KERNEL_STAGE). Enabling starts a new
  * measurement; reading synchronizes and returns the summed device time and
  * launch count. A model on the persistent stage kernel launches only
- * LPS_KERNEL_STAGE; the per-projection families apply to the chained kernels. */
+ * LPS_KERNEL_STAGE; the per-projection families apply to the chained kernels.
+ * LPS_EINVAL for a NULL model or output, or a kind above LPS_KERNEL_STAGE (the
+ * kinds after it name launches in the trace only). */
 #define LPS_KERNEL_QKV 0
 #define LPS_KERNEL_ATTN 1
 #define LPS_KERNEL_OPROJ 2
@@ -393,17 +409,19 @@ typedef struct {
  * per CTA; results are unchanged. LPS_EINVAL for capacity < 1. */
 int model_trace_enable(lps_model* m, int capacity);
 /* Synchronize, copy up to max_records records (launch order) into out, return
- * their count and the dropped count, and start a new recording. */
+ * their count and the dropped count, and start a new recording. LPS_EINVAL for
+ * NULL arguments or when tracing is not enabled. */
 int model_trace_read(lps_model* m, lps_trace_record* out, int max_records, int* n_records, uint64_t* dropped);
-/* Stop recording and release the buffer. */
+/* Stop recording and release the buffer (LPS_OK when tracing is already off). */
 int model_trace_disable(lps_model* m);
 
 /* ---- allocation-free attention ------------------------------------------ */
 
-/* The paper has no counterpart to this entry point. It serves callers that may
- * not allocate device memory once they run -- a serving loop with a hard
- * latency budget (allocation can synchronize the device), or a program whose
- * GPU memory is handed out once by its own pool. It runs the same split-K GQA
+/* The staged runtime on the pages has no counterpart to this entry point. It
+ * serves callers that may not allocate device memory once they run -- a
+ * serving loop with a hard latency budget (allocation can synchronize the
+ * device), or a program whose GPU memory is handed out once by its own pool.
+ * It runs the same split-K GQA
  * decode attention as the decode step, without a model: its scratch (partial
  * results and chunk counters) is one file-scope device array of
  * LPS_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until
