@@ -1462,6 +1462,23 @@ int enqueue_step_streams(lps_model* m, const int32_t* tok_host, const int32_t* t
 int prefill_init(lps_model* m, const char* FN) {
   PrefillState& P = m->pf;
   if (P.ready) return LPS_OK;
+  // an earlier call that failed part way: release what it made (once the
+  // clears it enqueued have run) before starting again
+  if (!P.st.empty() || !P.bd.empty())
+    for (int s = 0; s < m->N; ++s) CK(cudaStreamSynchronize(m->stream(s)), "stage stream");
+  for (auto& b : P.bd)
+    for (int i = 0; i < 2; ++i) {
+      if (b.ev_tx[i]) cudaEventDestroy(b.ev_tx[i]);
+      if (b.ev_rx[i]) cudaEventDestroy(b.ev_rx[i]);
+      dev_free(m, b.slot[i]);
+    }
+  P.bd.clear();
+  for (auto& F : P.st)
+    for (void* p : {static_cast<void*>(F.h), static_cast<void*>(F.q), static_cast<void*>(F.x),
+                    static_cast<void*>(F.xo), static_cast<void*>(F.xd), static_cast<void*>(F.apart),
+                    static_cast<void*>(F.gpart), static_cast<void*>(F.gcnt), static_cast<void*>(F.tok)})
+      dev_free(m, p);
+  P.st.clear();
   const lps_model_desc& d = m->d;
   const int N = m->N, E = d.n_embd, nq = d.n_q_heads, nkv = d.n_kv_heads, hd = d.head_dim, ffn = d.ffn;
   const int qw = nq * hd, rows_qkv = (nq + 2 * nkv) * hd;
