@@ -405,8 +405,8 @@ typedef struct {
 
 /* Record every launch of the following steps, up to `capacity` records (a
  * device buffer of 16 bytes per record, from the model's allocator; launches
- * past it are counted as dropped). Each kernel then does two extra atomics
- * per CTA; results are unchanged. LPS_EINVAL for capacity < 1. */
+ * past it are counted as dropped). Each kernel then does one extra atomic per
+ * CTA as it starts and one per warp as it ends; results are unchanged. LPS_EINVAL for capacity < 1. */
 int model_trace_enable(lps_model* m, int capacity);
 /* Synchronize, copy up to max_records records (launch order) into out, return
  * their count and the dropped count, and start a new recording. LPS_EINVAL for
