@@ -31,6 +31,15 @@ MUTANTS = {
     "softmax_not_normalised": ("for (int i = 0; i < hd; ++i) o[i] /= l;", ""),
     "boundary_in_f16_like": ("memcpy(hs, h, sizeof(float) * E);",
                              "memcpy(hs, h, sizeof(float) * E); if (s > 0) for (int i = 0; i < E; ++i) hs[i] = (float)(_Float16)hs[i];"),
+    # (every mutant stays inside its arrays: the pins load it into this process)
+    "rope_interleaved_pairs": ("double a = x[i], b = x[i + half];\n    x[i] = a * c - b * s;\n    x[i + half] = a * s + b * c;",
+                               "double a = x[2 * i], b = x[2 * i + 1];\n    x[2 * i] = a * c - b * s;\n    x[2 * i + 1] = a * s + b * c;"),
+    "attn_residual_dropped": ("orc_matvec(&L->wo, int8, o, y);\n  for (int i = 0; i < E; ++i) h[i] = (float)((double)h[i] + y[i]);",
+                              "orc_matvec(&L->wo, int8, o, y);\n  for (int i = 0; i < E; ++i) h[i] = (float)(y[i]);"),
+    "attn_scale_one_over_hd": ("double scale = 1.0 / sqrt((double)hd);", "double scale = 1.0 / (double)hd;"),
+    "norm_eps_outside_sqrt": ("sqrt(ss / n + eps)", "(sqrt(ss / n) + eps)"),
+    "embed_next_row": ("w_at(&m->embed, d->weight_int8, tokens[b], i)",
+                       "w_at(&m->embed, d->weight_int8, (tokens[b] + 1) % d->vocab, i)"),
 }
 
 
