@@ -38,6 +38,8 @@ MUTANTS = {
                               "orc_matvec(&L->wo, int8, o, y);\n  for (int i = 0; i < E; ++i) h[i] = (float)(y[i]);"),
     "attn_scale_one_over_hd": ("double scale = 1.0 / sqrt((double)hd);", "double scale = 1.0 / (double)hd;"),
     "norm_eps_outside_sqrt": ("sqrt(ss / n + eps)", "(sqrt(ss / n) + eps)"),
+    "softmax_sums_raw_scores": ("s[t] = exp(s[t] - m);\n    l += s[t];", "l += s[t];\n    s[t] = exp(s[t] - m);"),
+    "scores_against_v": ("acc += q[i] * bf16_value(K[(long)t * hd + i]);", "acc += q[i] * bf16_value(V[(long)t * hd + i]);"),
     "embed_next_row": ("w_at(&m->embed, d->weight_int8, tokens[b], i)",
                        "w_at(&m->embed, d->weight_int8, (tokens[b] + 1) % d->vocab, i)"),
 }
