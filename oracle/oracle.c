@@ -17,8 +17,9 @@
  *     3"; ninfer pipeline-stages.md, "Verification": split output equals one
  *     device byte for byte), so the step itself is the plain decoder below.
  *
- * The pages take the decoder's formulas as known. Readings used here (each is
- * listed with its reason in the design notes):
+ * The pages take the decoder's formulas as known. Readings used here, where
+ * they are silent: the standard forms of a decoder-only trunk (the pages name
+ * RMSNorm, RoPE, GQA and SwiGLU without defining them) --
  *   RMSNorm  xn_i = h_i * g_i / sqrt(mean(h^2) + eps), eps = 1e-5
  *   RoPE     rotate-half pairs (i, i + hd/2), angle pos * theta^(-2i/hd)
  *   attention over cache rows [0, pos] (the current row included), scale
