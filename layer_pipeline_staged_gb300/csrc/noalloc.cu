@@ -81,19 +81,22 @@ cudaError_t scratch_on(int dev, void** addr, int* num_sms) {
   return cudaSuccess;
 }
 
-bool encode_cache(CUtensorMap* map, const void* base, int hd, unsigned long long rows, int box_rows) {
-  static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
-  if (!enc) {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess) {
-      cudaGetLastError();
-      return false;
-    }
-    enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+// The driver's tensor-map encoder, looked up once per process (a function-local
+// static, so concurrent first calls initialise it once).
+PFN_cuTensorMapEncodeTiled_v12000 lookup_encoder() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess) {
+    cudaGetLastError();
+    return nullptr;
   }
+  return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+bool encode_cache(CUtensorMap* map, const void* base, int hd, unsigned long long rows, int box_rows) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 enc = lookup_encoder();
+  if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(hd), rows};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(hd) * 2};
   cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};

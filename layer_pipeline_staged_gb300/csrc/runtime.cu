@@ -506,19 +506,21 @@ bool place_matrix(lps_model* m, Uploader& up, int rows, int K, RowPtr row_ptr, R
 
 bool check_matrix(bool int8, const lps_matrix& x) { return x.w && (!int8 || x.scale); }
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda
+// link), looked up once per process (a function-local static: models bound on
+// several threads at once initialise it once).
+PFN_cuTensorMapEncodeTiled_v12000 lookup_tensor_map_encoder() {
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  cudaGetLastError();
+  return nullptr;
+}
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    else
-      cudaGetLastError();
-  }
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = lookup_tensor_map_encoder();
   return fn;
 }
 
